@@ -1,0 +1,134 @@
+"""Pins for the conv1d-backward and RMSNorm-backward oracles (CPU only)."""
+
+import numpy as np
+import pytest
+
+from oracle import (conv1d_causal_bwd_ref, conv1d_causal_fwd_ref, conv1d_step_bwd_ref, rmsnorm_bwd_ref,
+                    rmsnorm_fwd_ref)
+from tests._util import max_rel_err
+
+# ------------------------------------------------------------------ conv1d
+
+
+def _conv_inputs(rng, B=2, L=9, D=3, K=4):
+    return rng.standard_normal((B, L, D)), rng.standard_normal((D, K)), rng.standard_normal(D), rng.standard_normal((B, L, D))
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+def test_conv_forward_matches_numpy_convolve(K):
+    rng = np.random.default_rng(20 + K)
+    x, w, b, _ = _conv_inputs(rng, K=K)
+    out = conv1d_causal_fwd_ref(x, w, b)
+    for bb in range(2):
+        for d in range(3):
+            ref = np.convolve(x[bb, :, d], w[d, ::-1])[: x.shape[1]] + b[d]
+            np.testing.assert_allclose(out[bb, :, d], ref, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+def test_conv_backward_is_toeplitz_transpose(K):
+    """dx = T^T dout with T the causal Toeplitz matrix of each channel's filter (scipy.linalg.toeplitz)."""
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    rng = np.random.default_rng(30 + K)
+    x, w, _, dout = _conv_inputs(rng, L=11, K=K)
+    dx, dw, db = conv1d_causal_bwd_ref(dout, x, w)
+    L = x.shape[1]
+    for d in range(3):
+        col = np.zeros(L)
+        col[:K] = w[d, ::-1]  # out[t] = sum_j T[t, j] x[j], T[t, t-i] = w[K-1-i]
+        T = scipy_linalg.toeplitz(col, np.zeros(L))
+        for bb in range(2):
+            np.testing.assert_allclose(dx[bb, :, d], T.T @ dout[bb, :, d], rtol=1e-12, atol=1e-13)
+        # dw[d, k] = correlation of dout with x delayed by K-1-k
+        for k in range(K):
+            ref = sum(np.correlate(dout[bb, :, d], np.concatenate([np.zeros(K - 1 - k), x[bb, : L - (K - 1 - k), d]]))[0]
+                      for bb in range(2))
+            np.testing.assert_allclose(dw[d, k], ref, rtol=1e-12)
+    np.testing.assert_allclose(db, dout.sum(axis=(0, 1)), rtol=1e-13)
+
+
+def test_conv_backward_finite_differences():
+    rng = np.random.default_rng(40)
+    x, w, b, dout = _conv_inputs(rng, B=2, L=6, D=2, K=3)
+    dx, dw, db = conv1d_causal_bwd_ref(dout, x, w)
+    loss = lambda: float(np.sum(conv1d_causal_fwd_ref(x, w, b) * dout))
+    for arr, g in ((x, dx), (w, dw), (b, db)):
+        fd = np.empty_like(arr)
+        for idx in np.ndindex(arr.shape):
+            v0 = arr[idx]
+            arr[idx] = v0 + 1e-6
+            lp = loss()
+            arr[idx] = v0 - 1e-6
+            lm = loss()
+            arr[idx] = v0
+            fd[idx] = (lp - lm) / 2e-6
+        assert max_rel_err(g, fd) < 1e-8
+
+
+@pytest.mark.parametrize("K", [1, 4])
+def test_conv_full_sequence_equals_summed_step_formula(K):
+    """dw, db are the per-step contributions of the pages' step function summed over time;
+    with K=1 the input gradient is the step function's newest-tap gradient."""
+    rng = np.random.default_rng(50 + K)
+    x, w, _, dout = _conv_inputs(rng, B=2, L=8, D=3, K=K)
+    dx, dw, db = conv1d_causal_bwd_ref(dout, x, w)
+    dw_s = np.zeros_like(w)
+    db_s = np.zeros(3)
+    for bb in range(2):
+        state = np.zeros((3, K))
+        for t in range(x.shape[1]):
+            state = np.concatenate([state[:, 1:], x[bb, t][:, None]], axis=1)  # newest input at K-1
+            dx_t = conv1d_step_bwd_ref(dout[bb, t], state, w, dw_s, db_s)
+            if K == 1:
+                np.testing.assert_allclose(dx[bb, t], dx_t, rtol=1e-14)
+    np.testing.assert_allclose(dw, dw_s, rtol=1e-12)
+    np.testing.assert_allclose(db, db_s, rtol=1e-12)
+
+
+# ----------------------------------------------------------------- RMSNorm
+
+
+def test_rmsnorm_backward_finite_differences():
+    """FD through y = x*scale/sqrt(mean(x^2)+eps), rms recomputed from x, for dx and dscale."""
+    rng = np.random.default_rng(60)
+    R, H, eps = 3, 7, 1e-5
+    x = rng.standard_normal((R, H))
+    scale = 1 + 0.1 * rng.standard_normal(H)
+    dy = rng.standard_normal((R, H))
+    _, rms = rmsnorm_fwd_ref(x, scale, eps)
+    dx, dscale = rmsnorm_bwd_ref(dy, x, scale, rms)
+    loss = lambda: float(np.sum(rmsnorm_fwd_ref(x, scale, eps)[0] * dy))
+    for arr, g in ((x, dx), (scale, dscale)):
+        fd = np.empty_like(arr)
+        for idx in np.ndindex(arr.shape):
+            v0 = arr[idx]
+            arr[idx] = v0 + 1e-6
+            lp = loss()
+            arr[idx] = v0 - 1e-6
+            lm = loss()
+            arr[idx] = v0
+            fd[idx] = (lp - lm) / 2e-6
+        assert max_rel_err(g, fd) < 1e-8
+
+
+def test_rmsnorm_scale_invariance():
+    """With eps=0, y is invariant to scaling each row of x, so sum_i x_i dx_i = 0 per row."""
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((5, 33))
+    scale = 1 + 0.1 * rng.standard_normal(33)
+    dy = rng.standard_normal((5, 33))
+    _, rms = rmsnorm_fwd_ref(x, scale, 0.0)
+    dx, _ = rmsnorm_bwd_ref(dy, x, scale, rms)
+    np.testing.assert_allclose(np.sum(x * dx, axis=1), 0.0, atol=1e-12)
+
+
+def test_rmsnorm_rows_independent_and_dscale_sums_rows():
+    rng = np.random.default_rng(62)
+    x = rng.standard_normal((6, 10))
+    scale = rng.standard_normal(10)
+    dy = rng.standard_normal((6, 10))
+    rms = np.sqrt(np.mean(x * x, 1) + 1e-5)
+    dx, dscale = rmsnorm_bwd_ref(dy, x, scale, rms)
+    parts = [rmsnorm_bwd_ref(dy[i : i + 1], x[i : i + 1], scale, rms[i : i + 1]) for i in range(6)]
+    np.testing.assert_array_equal(np.concatenate([p[0] for p in parts]), dx)
+    np.testing.assert_allclose(sum(p[1] for p in parts), dscale, rtol=1e-13)

@@ -1,0 +1,286 @@
+"""Pins for the float64 selective-scan oracle (CPU only).
+
+Each test checks the oracle against something other than itself: an
+independent formulation (kernel/convolution form through cumulative sums, a
+bidiagonal linear solve), a closed form (L=1, A=0, constant inputs), the
+step-equivalence of chained calls, central finite differences and autodiff.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import scan_bwd_ref, scan_fwd_ref
+from tests._util import max_rel_err
+
+
+def _rand_inputs(rng, B=2, L=7, D=3, N=2, h0=True, A_scale=1.0):
+    x = rng.standard_normal((B, L, D))
+    delta = np.exp(rng.uniform(np.log(0.05), np.log(0.8), size=(B, L, D)))
+    z = rng.standard_normal((B, L, D))
+    Bm = rng.standard_normal((B, L, N))
+    Cm = rng.standard_normal((B, L, N))
+    A = -A_scale * rng.uniform(0.2, 3.0, size=(D, N))
+    Dv = rng.standard_normal(D)
+    dy = rng.standard_normal((B, L, D))
+    h0v = rng.standard_normal((B, D, N)) if h0 else None
+    return dict(x=x, delta=delta, A=A, Bm=Bm, Cm=Cm, Dv=Dv, z=z, dy=dy, h0=h0v)
+
+
+def _fwd(p, **kw):
+    return scan_fwd_ref(p["x"], p["delta"], p["A"], p["Bm"], p["Cm"], p["Dv"], p["z"], h0=p.get("h0"), **kw)
+
+
+def _bwd(p, **kw):
+    return scan_bwd_ref(p["x"], p["delta"], p["A"], p["Bm"], p["Cm"], p["Dv"], p["z"], p["dy"], h0=p.get("h0"), **kw)
+
+
+def _silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+# ---------------------------------------------------------------- forward pins
+
+def test_fwd_matches_kernel_form():
+    """h_t = sum_{s<=t} exp(A*(S_t - S_s)) * delta_s*B_s*x_s + exp(A*S_t)*h0, S = cumsum(delta)."""
+    rng = np.random.default_rng(1)
+    p = _rand_inputs(rng, B=2, L=9, D=3, N=3)
+    y, h_last, _ = _fwd(p)
+    S = np.cumsum(p["delta"], axis=1)  # [B,L,D]
+    B_, L, D = p["x"].shape
+    N = p["A"].shape[1]
+    h = np.zeros((B_, L, D, N))
+    for t in range(L):
+        decay = np.exp(p["A"][None, None] * (S[:, t, None, :, None] - S[:, : t + 1, :, None]))  # [B,s,D,N]
+        drive = (p["delta"][:, : t + 1] * p["x"][:, : t + 1])[..., None] * p["Bm"][:, : t + 1, None, :]
+        h[:, t] = np.sum(decay * drive, axis=1) + np.exp(p["A"][None] * S[:, t, :, None]) * p["h0"]
+    y_ref = (np.einsum("btdn,btn->btd", h, p["Cm"]) + p["Dv"] * p["x"]) * _silu(p["z"])
+    assert max_rel_err(y, y_ref) < 1e-12
+    assert max_rel_err(h_last, h[:, -1]) < 1e-12
+
+
+def test_fwd_matches_bidiagonal_solve():
+    """For each (b,d,n) the states solve the lower-bidiagonal system h_t - a_t h_{t-1} = delta_t B_t x_t."""
+    rng = np.random.default_rng(2)
+    p = _rand_inputs(rng, B=1, L=8, D=2, N=2)
+    _, h_last, ckpt = _fwd(p, chunk=1)  # chunk=1: ckpt[..., c, :] = h_{c-1}
+    L = p["x"].shape[1]
+    for d in range(2):
+        for n in range(2):
+            a = np.exp(p["delta"][0, :, d] * p["A"][d, n])
+            M = np.eye(L) - np.diag(a[1:], k=-1)
+            rhs = p["delta"][0, :, d] * p["Bm"][0, :, n] * p["x"][0, :, d]
+            rhs[0] += a[0] * p["h0"][0, d, n]
+            h = np.linalg.solve(M, rhs)
+            assert abs(h[-1] - h_last[0, d, n]) <= 1e-12 * max(1.0, abs(h[-1]))
+            np.testing.assert_allclose(ckpt[0, d, 1:, n], h[:-1], rtol=1e-12, atol=1e-14)
+            assert ckpt[0, d, 0, n] == p["h0"][0, d, n]
+
+
+def test_fwd_L1_closed_form():
+    rng = np.random.default_rng(3)
+    p = _rand_inputs(rng, B=2, L=1, D=4, N=3)
+    y, h_last, _ = _fwd(p)
+    a = np.exp(p["delta"][:, 0, :, None] * p["A"][None])
+    h1 = a * p["h0"] + (p["delta"][:, 0] * p["x"][:, 0])[..., None] * p["Bm"][:, 0, None, :]
+    y1 = (np.sum(p["Cm"][:, 0, None, :] * h1, -1) + p["Dv"] * p["x"][:, 0]) * _silu(p["z"][:, 0])
+    np.testing.assert_allclose(h_last, h1, rtol=1e-14)
+    np.testing.assert_allclose(y[:, 0], y1, rtol=1e-13)
+
+
+def test_fwd_A_zero_is_cumsum():
+    """A=0: h_t = h0 + cumsum_t(delta*B*x); A=-1e-9 stays within ~1e-8 of it."""
+    rng = np.random.default_rng(4)
+    p = _rand_inputs(rng, B=2, L=20, D=3, N=4)
+    p["A"] = np.zeros_like(p["A"])
+    _, h_last, ckpt = _fwd(p, chunk=5)
+    drive = (p["delta"] * p["x"])[..., None] * p["Bm"][:, :, None, :]  # [B,L,D,N]
+    cs = np.cumsum(drive, axis=1) + p["h0"][:, None]
+    np.testing.assert_allclose(h_last, cs[:, -1], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ckpt[:, :, 1:, :], np.moveaxis(cs[:, 4:-1:5], 1, 2), rtol=1e-12, atol=1e-12)
+    p["A"] = np.full_like(p["A"], -1e-9)
+    _, h_small, _ = _fwd(p)
+    assert max_rel_err(h_small, cs[:, -1]) < 1e-7
+
+
+def test_fwd_constant_input_geometric_series():
+    """Constant delta, x, B over time: h_t = a^(t+1) h0 + v (1 - a^(t+1)) / (1 - a)."""
+    rng = np.random.default_rng(5)
+    B_, L, D, N = 1, 30, 2, 3
+    p = _rand_inputs(rng, B=B_, L=L, D=D, N=N)
+    p["delta"][:] = p["delta"][:, :1]
+    p["x"][:] = p["x"][:, :1]
+    p["Bm"][:] = p["Bm"][:, :1]
+    _, h_last, _ = _fwd(p)
+    a = np.exp(p["delta"][:, 0, :, None] * p["A"][None])
+    v = (p["delta"][:, 0] * p["x"][:, 0])[..., None] * p["Bm"][:, 0, None, :]
+    h_ref = a ** L * p["h0"] + v * (1 - a ** L) / (1 - a)
+    np.testing.assert_allclose(h_last, h_ref, rtol=1e-11)
+
+
+def test_fwd_step_equivalence_and_segments():
+    """L single-step calls chained through h_last -> h0 equal one call; so does a 2-way split."""
+    rng = np.random.default_rng(6)
+    p = _rand_inputs(rng, B=2, L=11, D=3, N=2)
+    y, h_last, _ = _fwd(p)
+    h = p["h0"]
+    ys = []
+    for t in range(11):
+        q = {k: (v[:, t : t + 1] if k in ("x", "delta", "z", "Bm", "Cm", "dy") else v) for k, v in p.items()}
+        q["h0"] = h
+        yt, h, _ = _fwd(q)
+        ys.append(yt)
+    np.testing.assert_array_equal(np.concatenate(ys, axis=1), y)
+    np.testing.assert_array_equal(h, h_last)
+    for cut in (1, 4, 10):
+        a = {k: (v[:, :cut] if k in ("x", "delta", "z", "Bm", "Cm", "dy") else v) for k, v in p.items()}
+        b = {k: (v[:, cut:] if k in ("x", "delta", "z", "Bm", "Cm", "dy") else v) for k, v in p.items()}
+        ya, ha, _ = _fwd(a)
+        b["h0"] = ha
+        yb, hb, _ = _fwd(b)
+        np.testing.assert_array_equal(np.concatenate([ya, yb], 1), y)
+        np.testing.assert_array_equal(hb, h_last)
+
+
+def test_fwd_checkpoints_are_prefix_states():
+    rng = np.random.default_rng(7)
+    p = _rand_inputs(rng, B=2, L=13, D=2, N=2)
+    _, _, ckpt = _fwd(p, chunk=4)
+    assert ckpt.shape == (2, 2, 4, 2)
+    np.testing.assert_array_equal(ckpt[:, :, 0], p["h0"])
+    for c in range(1, 4):
+        q = {k: (v[:, : 4 * c] if k in ("x", "delta", "z", "Bm", "Cm", "dy") else v) for k, v in p.items()}
+        _, hc, _ = _fwd(q)
+        np.testing.assert_array_equal(ckpt[:, :, c], hc)
+    p["h0"] = None
+    _, _, ck0 = _fwd(p, chunk=4)
+    assert np.all(ck0[:, :, 0] == 0)
+
+
+def test_fwd_C_zero_gives_skip_path():
+    rng = np.random.default_rng(8)
+    p = _rand_inputs(rng)
+    p["Cm"] = np.zeros_like(p["Cm"])
+    y, _, _ = _fwd(p)
+    np.testing.assert_allclose(y, p["Dv"] * p["x"] * _silu(p["z"]), rtol=1e-14)
+
+
+# --------------------------------------------------------------- backward pins
+
+def _loss(p):
+    y, _, _ = _fwd(p)
+    return float(np.sum(y * p["dy"]))
+
+
+@pytest.mark.parametrize("with_h0", [True, False])
+def test_bwd_central_finite_differences(with_h0):
+    rng = np.random.default_rng(10 + with_h0)
+    p = _rand_inputs(rng, B=2, L=6, D=3, N=2, h0=with_h0)
+    g = _bwd(p)
+    names = {"x": "dx", "delta": "ddelta", "z": "dz", "A": "dA", "Bm": "dB", "Cm": "dC", "Dv": "dD"}
+    if with_h0:
+        names["h0"] = "dh0"
+    for name, gname in names.items():
+        base = p[name]
+        fd = np.empty_like(base)
+        for idx in np.ndindex(base.shape):
+            v0 = base[idx]
+            hstep = 1e-6 * max(1.0, abs(v0))
+            base[idx] = v0 + hstep
+            lp = _loss(p)
+            base[idx] = v0 - hstep
+            lm = _loss(p)
+            base[idx] = v0
+            fd[idx] = (lp - lm) / (2 * hstep)
+        err = max_rel_err(g[gname], fd)
+        assert err < 1e-7, f"{gname}: FD rel err {err:.2e}"
+    if not with_h0:
+        # the gradient w.r.t. a zero initial state is still defined: FD through an explicit zero h0
+        q = dict(p)
+        q["h0"] = np.zeros((2, 3, 2))
+        g2 = _bwd(q)
+        np.testing.assert_allclose(g["dh0"], g2["dh0"], rtol=1e-14, atol=0)
+
+
+def test_bwd_matches_torch_autograd():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(12)
+    p = _rand_inputs(rng, B=2, L=9, D=4, N=3)
+    g = _bwd(p)
+    T = {k: torch.tensor(v, dtype=torch.float64, requires_grad=(k != "dy")) for k, v in p.items()}
+    h = T["h0"]
+    ys = []
+    for t in range(9):
+        a = torch.exp(T["delta"][:, t, :, None] * T["A"][None])
+        h = a * h + (T["delta"][:, t] * T["x"][:, t])[..., None] * T["Bm"][:, t, None, :]
+        s = (h * T["Cm"][:, t, None, :]).sum(-1) + T["Dv"] * T["x"][:, t]
+        ys.append(s * torch.nn.functional.silu(T["z"][:, t]))
+    loss = (torch.stack(ys, 1) * T["dy"]).sum()
+    loss.backward()
+    for k, gk in {"x": "dx", "delta": "ddelta", "z": "dz", "A": "dA", "Bm": "dB", "Cm": "dC", "Dv": "dD", "h0": "dh0"}.items():
+        assert max_rel_err(g[gk], T[k].grad.numpy()) < 1e-12, gk
+
+
+def test_bwd_L1_closed_form():
+    rng = np.random.default_rng(13)
+    p = _rand_inputs(rng, B=2, L=1, D=3, N=4)
+    g = _bwd(p)
+    d, x, z, dy = p["delta"][:, 0], p["x"][:, 0], p["z"][:, 0], p["dy"][:, 0]
+    Bv, Cv, A, h0 = p["Bm"][:, 0], p["Cm"][:, 0], p["A"], p["h0"]
+    sig = 1 / (1 + np.exp(-z))
+    a = np.exp(d[..., None] * A[None])
+    h1 = a * h0 + (d * x)[..., None] * Bv[:, None, :]
+    s = np.sum(Cv[:, None, :] * h1, -1) + p["Dv"] * x
+    ds = dy * z * sig
+    np.testing.assert_allclose(g["dz"][:, 0], dy * s * sig * (1 + z * (1 - sig)), rtol=1e-12)
+    np.testing.assert_allclose(g["dA"], np.sum(ds[..., None] * Cv[:, None, :] * h0 * a * d[..., None], 0), rtol=1e-12)
+    np.testing.assert_allclose(g["dB"][:, 0], np.sum((ds * d * x)[..., None] * Cv[:, None, :], 1), rtol=1e-12)
+    np.testing.assert_allclose(g["dC"][:, 0], np.sum(ds[..., None] * h1, 1), rtol=1e-12)
+    np.testing.assert_allclose(g["dD"], np.sum(ds * x, 0), rtol=1e-12)
+    np.testing.assert_allclose(g["dx"][:, 0], ds * (d * np.sum(Cv * Bv, -1)[:, None] + p["Dv"]), rtol=1e-12)
+    np.testing.assert_allclose(g["dh0"], ds[..., None] * Cv[:, None, :] * a, rtol=1e-12)
+
+
+def test_bwd_A_zero_reverse_cumsum():
+    """A=0: G_t = reverse-cumsum(ds*C) and dA = sum_t delta_t * h_{t-1} * G_t."""
+    rng = np.random.default_rng(14)
+    p = _rand_inputs(rng, B=2, L=12, D=3, N=2)
+    p["A"] = np.zeros_like(p["A"])
+    g = _bwd(p)
+    ds = p["dy"] * _silu(p["z"])
+    dsC = ds[..., None] * p["Cm"][:, :, None, :]
+    G = np.cumsum(dsC[:, ::-1], axis=1)[:, ::-1]
+    drive = (p["delta"] * p["x"])[..., None] * p["Bm"][:, :, None, :]
+    h = np.cumsum(drive, axis=1) + p["h0"][:, None]
+    h_prev = np.concatenate([p["h0"][:, None], h[:, :-1]], axis=1)
+    np.testing.assert_allclose(g["dA"], np.sum(p["delta"][..., None] * h_prev * G, axis=(0, 1)), rtol=1e-11)
+    np.testing.assert_allclose(g["dh0"], G[:, 0], rtol=1e-12)
+    np.testing.assert_allclose(g["dB"], np.sum(G * (p["delta"] * p["x"])[..., None], axis=2), rtol=1e-11)
+
+
+def test_bwd_segment_chaining():
+    """Backward of a split sequence, chained through h0 (forward) and dh_last (backward), equals one call."""
+    rng = np.random.default_rng(15)
+    p = _rand_inputs(rng, B=2, L=10, D=3, N=2)
+    full = _bwd(p)
+    cut = 6
+    seq = ("x", "delta", "z", "Bm", "Cm", "dy")
+    a = {k: (v[:, :cut] if k in seq else v) for k, v in p.items()}
+    b = {k: (v[:, cut:] if k in seq else v) for k, v in p.items()}
+    _, ha, _ = _fwd(a)
+    b["h0"] = ha
+    gb = _bwd(b)
+    ga = _bwd(a, dh_last=gb["dh0"])
+    for k in ("dx", "ddelta", "dz", "dB", "dC"):
+        np.testing.assert_allclose(np.concatenate([ga[k], gb[k]], 1), full[k], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(ga["dA"] + gb["dA"], full["dA"], rtol=1e-12)
+    np.testing.assert_allclose(ga["dD"] + gb["dD"], full["dD"], rtol=1e-12)
+    np.testing.assert_allclose(ga["dh0"], full["dh0"], rtol=1e-12)
+
+
+def test_bwd_segment_recompute_is_exact():
+    rng = np.random.default_rng(16)
+    p = _rand_inputs(rng, B=2, L=17, D=3, N=2)
+    g1 = _bwd(p, segment=17)
+    g2 = _bwd(p, segment=4)
+    for k in g1:
+        np.testing.assert_array_equal(g1[k], g2[k])
