@@ -1,0 +1,181 @@
+/*
+ * ssscan.h — C ABI of libssscan.so: the Mamba selective-scan forward and
+ * backward, the depthwise causal conv1d backward and the RMSNorm backward,
+ * written for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor argument is a caller-owned DEVICE pointer to a dense,
+ *   row-major (C-contiguous) buffer; strided views are not accepted (a strided
+ *   view silently read as contiguous is the bug the rustytorch backward_cuda
+ *   commit message reports: "cuda_matmul reads raw GPU storage by shape.dims()
+ *   ignoring strides/offset").  The library never allocates or frees memory
+ *   in these calls; scratch comes from the caller's `workspace`, sized by the
+ *   matching *_workspace_size() query.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Calls only enqueue work on it and return; device-side failures
+ *   surface at the caller's next synchronisation or through ss_device_status().
+ * - Return value: SS_OK (0) or a negative SS_ERR_* code.  Arguments are
+ *   validated on the host before anything is launched; on an error nothing
+ *   is launched and no output is touched.  ss_strerror() gives the text.
+ * - Activations (x, delta, z, dy, y, Bm, Cm of the scan; x of conv1d; x, dy of
+ *   RMSNorm) are fp32 (SS_F32) or bf16 (SS_BF16) as given by `dtype`; states,
+ *   checkpoints, A, D, weights and every gradient are fp32.
+ * - Gradients of parameters ACCUMULATE (+=): dA, dD, dw, db, dscale.
+ *   Gradients of activations are OVERWRITTEN (=): dx, ddelta, dz, dB, dC,
+ *   dh0 — the convention of mamba-rs backward_ops.rs ("accumulated" weight,
+ *   bias and scale gradients; "overwritten" input gradients).
+ * - Reductions are deterministic: fixed-order trees over per-block partials,
+ *   no atomics.  Two identical calls give bitwise-identical results.
+ */
+#ifndef SSSCAN_H
+#define SSSCAN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define SS_OK 0
+#define SS_ERR_NULL (-1)        /* a required pointer is NULL */
+#define SS_ERR_DIM (-2)         /* a size is <= 0, or out of the supported range */
+#define SS_ERR_UNSUPPORTED (-3) /* N not in {4,8,16}, unknown dtype, d_conv not in 1..4, chunk not a multiple of 16 */
+#define SS_ERR_ALIGN (-4)       /* a pointer is not 16-byte aligned, or D / dim not a multiple of 8 */
+#define SS_ERR_WORKSPACE (-5)   /* workspace NULL or smaller than the *_workspace_size() query */
+#define SS_ERR_CUDA (-6)        /* a CUDA runtime call or kernel launch failed */
+#define SS_ERR_DEVICE (-7)      /* a kernel gave up on a bounded wait (ss_device_status) */
+
+/* activation dtypes */
+#define SS_F32 0
+#define SS_BF16 1
+
+/* Human-readable text of a status code (static storage, never NULL). */
+const char* ss_strerror(int code);
+
+/*
+ * Number of checkpoints the forward writes: ceil(L / chunk).
+ */
+int ss_scan_num_chunks(int L, int chunk);
+
+/*
+ * ss_scan_fwd — selective-scan forward.
+ *
+ * The diagonal selective SSM trained by backpropagation through time in the
+ * rustytorch MambaBlock ("the inherently sequential scan") and mamba-rs
+ * ("BPTT through SSM state"); per batch b, channel d, state n, step t:
+ *     a_t   = exp(delta_t[d] * A[d,n])
+ *     h_t   = a_t * h_{t-1} + delta_t[d] * B_t[n] * x_t[d]        (h_{-1} = h0, or 0)
+ *     y_t[d] = (sum_n C_t[n] * h_t[d,n] + D[d] * x_t[d]) * silu(z_t[d])
+ *
+ *   x, delta, z : [B, L, D]  activations (dtype); delta is already positive (post-softplus)
+ *   A           : [D, N]     fp32 (negative for a decaying state)
+ *   Bm, Cm      : [B, L, N]  activations (dtype), shared by all D channels
+ *   Dv          : [D]        fp32 skip weight
+ *   h0          : [B, D, N]  fp32 initial state, or NULL for zeros
+ *   y           : [B, L, D]  output (dtype; bf16 is rounded to nearest even)
+ *   ckpt        : [B, D, ceil(L/chunk), N] fp32 output: ckpt[b,d,c,:] is the
+ *                 state entering step c*chunk (c = 0 holds h0 or zeros).  The
+ *                 backward rebuilds every other state from these.
+ *   h_last      : [B, D, N]  fp32 final state h_{L-1}, or NULL
+ *   chunk       : checkpoint interval, a positive multiple of 16
+ *   N           : 4, 8 or 16;  D: a multiple of 8
+ * Alignment: every pointer 16-byte aligned.
+ */
+int ss_scan_fwd(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm,
+                const float* Dv, const void* z, const float* h0,
+                void* y, float* ckpt, float* h_last,
+                int B, int L, int D, int N, int chunk, int dtype, void* stream);
+
+/*
+ * Workspace bytes ss_scan_bwd needs for these sizes (0 on invalid sizes).
+ */
+size_t ss_scan_bwd_workspace_size(int B, int L, int D, int N, int chunk, int dtype);
+
+/*
+ * ss_scan_bwd — reverse-mode gradient of  sum(y * dy) + sum(h_last * dh_last)
+ * through ss_scan_fwd (backpropagation through time through the SSM state).
+ *
+ * Inputs are those of the forward plus
+ *   ckpt     : [B, D, ceil(L/chunk), N] the forward's checkpoints, same chunk
+ *   dy       : [B, L, D] activations (dtype): dL/dy
+ *   dh_last  : [B, D, N] fp32 gradient arriving on the final state, or NULL (zero)
+ * Outputs (fp32):
+ *   dx, ddelta, dz : [B, L, D]   overwritten
+ *   dB, dC         : [B, L, N]   overwritten (summed over the D channels)
+ *   dA             : [D, N]      accumulated (+=, summed over batch and time)
+ *   dD             : [D]         accumulated (+=)
+ *   dh0            : [B, D, N]   overwritten, or NULL to skip
+ * with, for G_t = dL/dh_t = ds_t*C_t + a_{t+1}*G_{t+1},  ds_t = dy_t*silu(z_t):
+ *   q_t = G_t*a_t*h_{t-1};  ddelta_t = sum_n (q_t*A + G_t*B_t*x_t);
+ *   dx_t = ds_t*D + delta_t*sum_n G_t*B_t;  dz_t = dy_t*s_t*silu'(z_t);
+ *   dA += sum q_t*delta_t;  dB_t = sum_d G_t*delta_t*x_t;  dC_t = sum_d ds_t*h_t;
+ *   dD += sum ds_t*x_t;  dh0 = a_0*G_0.
+ * The states are rebuilt chunk by chunk from `ckpt`, never stored in full.
+ * workspace: device scratch of at least ss_scan_bwd_workspace_size() bytes,
+ *   16-byte aligned, contents need not be initialised.
+ */
+int ss_scan_bwd(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm,
+                const float* Dv, const void* z, const float* ckpt, const void* dy, const float* dh_last,
+                float* dx, float* ddelta, float* dz, float* dA, float* dB, float* dC, float* dD, float* dh0,
+                int B, int L, int D, int N, int chunk, int dtype,
+                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Workspace bytes conv1d_causal_bwd needs (0 on invalid sizes).
+ */
+size_t conv1d_causal_bwd_workspace_size(int B, int L, int D, int d_conv);
+
+/*
+ * conv1d_causal_bwd — backward of the depthwise causal conv1d
+ *     out[b,t,d] = bias[d] + sum_k w[d,k] * x[b, t-(d_conv-1)+k, d]      (x at t<0 is 0)
+ * whose per-channel shift register holds the newest input at tap d_conv-1
+ * (mamba-rs backward_ops.rs, backward_conv1d_step).  Full-sequence gradient:
+ *   dout : [B, L, D] fp32, dL/dout (the gradient after the SiLU backward)
+ *   x    : [B, L, D] conv input (x_dtype: SS_F32 or SS_BF16)
+ *   w    : [D, d_conv] fp32
+ *   dx   : [B, L, D] fp32, overwritten: dx[s] = sum_k dout[s+d_conv-1-k] * w[k]
+ *   dw   : [D, d_conv] fp32, accumulated: += sum_{b,t} dout[t] * x[t-(d_conv-1)+k]
+ *   db   : [D] fp32, accumulated: += sum_{b,t} dout[t]
+ * d_conv in 1..4; D a multiple of 8; pointers 16-byte aligned.  dw and db
+ * equal the pages' per-step contributions summed over every step.
+ */
+int conv1d_causal_bwd(const float* dout, const void* x, const float* w,
+                      float* dx, float* dw, float* db,
+                      int B, int L, int D, int d_conv, int x_dtype,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Workspace bytes rmsnorm_bwd needs (0 on invalid sizes).
+ */
+size_t rmsnorm_bwd_workspace_size(int rows, int dim);
+
+/*
+ * rmsnorm_bwd — backward of y[r,i] = x[r,i] * scale[i] / rms[r]
+ * (mamba-rs backward_ops.rs, backward_rms_norm):
+ *   inv = 1/rms[r];  dot = inv^2 * sum_i dy*scale*x
+ *   dx[r,i]    = inv * (scale[i]*dy[r,i] - x[r,i]*dot/dim)     overwritten
+ *   dscale[i] += sum_r dy[r,i]*x[r,i]*inv                        accumulated
+ *   dy, x : [rows, dim] (dtype);  scale : [dim] fp32;  rms : [rows] fp32, the
+ *   root mean square saved by the forward (not its inverse; eps already inside);
+ *   dx : [rows, dim] fp32;  dscale : [dim] fp32.
+ * dim a multiple of 8 and at most 32768; pointers 16-byte aligned.
+ */
+int rmsnorm_bwd(const void* dy, const void* x, const float* scale, const float* rms,
+                float* dx, float* dscale, int rows, int dim, int dtype,
+                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * ss_device_status — synchronises `stream`, then reads and clears the
+ * library's device-side error word.  Returns SS_OK, or SS_ERR_DEVICE when a
+ * kernel gave up on a bounded wait for its own asynchronous copies since the
+ * last call (its outputs are then invalid), or SS_ERR_CUDA.
+ */
+int ss_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSSCAN_H */

@@ -1,0 +1,180 @@
+// Depthwise causal conv1d backward (conv1d_causal_bwd) for sm_103a.
+//
+//   out[t,d] = bias[d] + sum_k w[d,k] x[t-(K-1)+k, d]     (newest input at tap K-1)
+//   dx[s,d]  = sum_j dout[s+j, d] w[d, K-1-j]             (terms past the end dropped)
+//   dw[d,k] += sum_{b,t} dout[t,d] x[t-(K-1)+k, d],   db[d] += sum_{b,t} dout[t,d]
+//
+// A thread owns 4 adjacent channels (one 16-byte fp32 vector of dout per
+// step) over a 64-step tile of one batch row and slides two K-wide register
+// windows along time: dout ahead of the output step (for dx) and x behind it
+// (for dw).  Each CTA loops over several (batch, tile) pairs, keeping dw / db
+// in registers, and writes one partial per CTA row; conv_reduce_kernel adds
+// the partials in fixed order into dw / db.  HBM traffic is one read of dout
+// and x plus one write of dx (the K-1 halo steps per tile come from L2).
+#include "common.cuh"
+
+namespace {
+
+using namespace ssk;
+
+constexpr int kCTile = 64;     // time steps per tile
+constexpr int kCThreads = 128;  // threads per CTA: 512 channels
+
+template <typename T>
+__device__ __forceinline__ float4 ld_x4(const T* p);
+template <>
+__device__ __forceinline__ float4 ld_x4<float>(const float* p) { return *reinterpret_cast<const float4*>(p); }
+template <>
+__device__ __forceinline__ float4 ld_x4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+}
+
+__device__ __forceinline__ float4 f4fma(float4 a, float4 b, float4 c) {
+  return make_float4(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y), fmaf(a.z, b.z, c.z), fmaf(a.w, b.w, c.w));
+}
+__device__ __forceinline__ float4 f4add(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+__device__ __forceinline__ float4 f4z() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+
+template <int K, typename T>
+__global__ void __launch_bounds__(kCThreads) conv_bwd_kernel(const float* __restrict__ dout, const T* __restrict__ x,
+                                                             const float* __restrict__ w, float* __restrict__ dx,
+                                                             float* __restrict__ ws, int B, int L, int D) {
+  const int d = (blockIdx.x * kCThreads + threadIdx.x) * 4;
+  const bool valid = d < D;  // D % 8 == 0, so all four channels are in range
+  const int ntt = (L + kCTile - 1) / kCTile;
+  float4 wk[K];  // wk[k] = w[d..d+3, k]
+#pragma unroll
+  for (int k = 0; k < K; ++k)
+    wk[k] = valid ? make_float4(w[(size_t)d * K + k], w[(size_t)(d + 1) * K + k], w[(size_t)(d + 2) * K + k],
+                                w[(size_t)(d + 3) * K + k])
+                  : f4z();
+  float4 dw[K], db = f4z();
+#pragma unroll
+  for (int k = 0; k < K; ++k) dw[k] = f4z();
+
+  if (valid) {
+    for (int bt = blockIdx.y; bt < B * ntt; bt += gridDim.y) {
+      const int b = bt / ntt, t0 = (bt % ntt) * kCTile;
+      const int t1 = min(L, t0 + kCTile);
+      const float* g = dout + (size_t)b * L * D + d;
+      const T* xb = x + (size_t)b * L * D + d;
+      float4 gw[K], xw[K];  // gw[j] = dout[s+j], xw[k] = x[s-(K-1)+k]
+#pragma unroll
+      for (int j = 0; j < K - 1; ++j) {
+        const int t = t0 + j;
+        gw[j + 1] = t < L ? *reinterpret_cast<const float4*>(g + (size_t)t * D) : f4z();
+        const int tx = t0 - (K - 1) + j;
+        xw[j + 1] = tx >= 0 ? ld_x4(xb + (size_t)tx * D) : f4z();
+      }
+#pragma unroll 4
+      for (int s = t0; s < t1; ++s) {
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) {
+          gw[j] = gw[j + 1];
+          xw[j] = xw[j + 1];
+        }
+        const int tg = s + K - 1;
+        gw[K - 1] = tg < L ? *reinterpret_cast<const float4*>(g + (size_t)tg * D) : f4z();
+        xw[K - 1] = ld_x4(xb + (size_t)s * D);
+        float4 acc = f4z();
+#pragma unroll
+        for (int j = 0; j < K; ++j) acc = f4fma(gw[j], wk[K - 1 - j], acc);
+        *reinterpret_cast<float4*>(dx + ((size_t)b * L + s) * D + d) = acc;
+#pragma unroll
+        for (int k = 0; k < K; ++k) dw[k] = f4fma(gw[0], xw[k], dw[k]);
+        db = f4add(db, gw[0]);
+      }
+    }
+    float* o = ws + ((size_t)blockIdx.y * D + d) * (K + 1);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) o[c * (K + 1) + k] = c == 0 ? dw[k].x : c == 1 ? dw[k].y : c == 2 ? dw[k].z : dw[k].w;
+      o[c * (K + 1) + K] = c == 0 ? db.x : c == 1 ? db.y : c == 2 ? db.z : db.w;
+    }
+  }
+}
+
+// dw[d,k] += sum_g ws[g][d][k];  db[d] += sum_g ws[g][d][K]
+__global__ void conv_reduce_kernel(const float* __restrict__ ws, float* dw, float* db, int D, int K, int gy) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int per = K + 1;
+  if (i >= D * per) return;
+  float acc = 0.f;
+  for (int g = 0; g < gy; ++g) acc += ws[(size_t)g * D * per + i];
+  const int d = i / per, k = i % per;
+  if (k < K) dw[(size_t)d * K + k] += acc;
+  else db[d] += acc;
+}
+
+struct ConvPlan {
+  int gx, gy;
+  size_t bytes;
+};
+
+inline ConvPlan conv_plan(int B, int L, int D, int K) {
+  ConvPlan p;
+  p.gx = (D / 4 + kCThreads - 1) / kCThreads;
+  const long long pairs = (long long)B * ((L + kCTile - 1) / kCTile);
+  long long cap = 2048 / p.gx;
+  if (cap < 1) cap = 1;
+  p.gy = (int)(pairs < cap ? pairs : cap);
+  p.bytes = (size_t)p.gy * D * (K + 1) * sizeof(float);
+  return p;
+}
+
+int conv_validate(int B, int L, int D, int K, int x_dtype) {
+  if (B <= 0 || L <= 0 || D <= 0 || K <= 0) return SS_ERR_DIM;
+  if (K > 4) return SS_ERR_UNSUPPORTED;
+  if (x_dtype != SS_F32 && x_dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  if (D % 8 != 0) return SS_ERR_ALIGN;
+  if ((long long)B * ((L + kCTile - 1) / kCTile) >= (1ll << 31)) return SS_ERR_DIM;
+  return SS_OK;
+}
+
+template <int K, typename T>
+int conv_launch(const float* dout, const void* x, const float* w, float* dx, float* dw, float* db, int B, int L, int D,
+                float* ws, const ConvPlan& pl, cudaStream_t s) {
+  conv_bwd_kernel<K, T><<<dim3(pl.gx, pl.gy), kCThreads, 0, s>>>(dout, static_cast<const T*>(x), w, dx, ws, B, L, D);
+  if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+  const int n = D * (K + 1);
+  conv_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(ws, dw, db, D, K, pl.gy);
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" size_t conv1d_causal_bwd_workspace_size(int B, int L, int D, int d_conv) {
+  if (conv_validate(B, L, D, d_conv, SS_F32) != SS_OK) return 0;
+  return conv_plan(B, L, D, d_conv).bytes;
+}
+
+extern "C" int conv1d_causal_bwd(const float* dout, const void* x, const float* w, float* dx, float* dw, float* db, int B,
+                                 int L, int D, int d_conv, int x_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  if (!dout || !x || !w || !dx || !dw || !db) return SS_ERR_NULL;
+  const int v = conv_validate(B, L, D, d_conv, x_dtype);
+  if (v != SS_OK) return v;
+  const void* ptrs[] = {dout, x, w, dx, dw, db};
+  for (const void* q : ptrs)
+    if (!ssh::aligned16(q)) return SS_ERR_ALIGN;
+  const ConvPlan pl = conv_plan(B, L, D, d_conv);
+  if (workspace == nullptr || ws_bytes < pl.bytes) return SS_ERR_WORKSPACE;
+  if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
+  float* ws = static_cast<float*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (x_dtype == SS_F32) {
+    switch (d_conv) {
+      case 1: return conv_launch<1, float>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
+      case 2: return conv_launch<2, float>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
+      case 3: return conv_launch<3, float>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
+      default: return conv_launch<4, float>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
+    }
+  }
+  switch (d_conv) {
+    case 1: return conv_launch<1, __nv_bfloat16>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
+    case 2: return conv_launch<2, __nv_bfloat16>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
+    case 3: return conv_launch<3, __nv_bfloat16>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
+    default: return conv_launch<4, __nv_bfloat16>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
+  }
+}

@@ -1,0 +1,169 @@
+// RMSNorm backward (rmsnorm_bwd) for sm_103a.
+//
+//   inv = 1/rms_r;  dot_r = inv^2 sum_i dy*scale*x
+//   dx[r,i] = inv (scale_i dy[r,i] - x[r,i] dot_r / dim);   dscale_i += sum_r dy x inv
+//
+// A CTA of T = ceil(dim / (8 VPT)) threads walks rows r = blockIdx.x, +gridDim.x, ...
+// Each thread owns VPT groups of 8 consecutive columns (16-byte bf16 or two
+// 16-byte fp32 loads), keeps scale and its dscale partial in registers, and
+// prefetches the next row while the current row's dot product is reduced
+// (warp shuffles, then one shared-memory exchange whose buffer alternates
+// with the row parity, so one barrier per row suffices).  Per-CTA dscale
+// partials are added in fixed order by rms_reduce_kernel.
+#include "common.cuh"
+
+namespace {
+
+using namespace ssk;
+
+constexpr int kRmsMaxThreads = 1024;
+constexpr int kRmsMaxDim = 32768;
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
+                                                                 const float* __restrict__ scale,
+                                                                 const float* __restrict__ rms, float* __restrict__ dx,
+                                                                 float* __restrict__ ws, int rows, int dim) {
+  __shared__ float red[2][32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
+  float sc[VPT][8], acc[VPT][8], gy[VPT][8], xv[VPT][8], gyn[VPT][8], xvn[VPT][8];
+  bool col_ok[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = (v * blockDim.x + tid) * 8;
+    col_ok[v] = c < dim;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sc[v][e] = col_ok[v] ? scale[c + e] : 0.f;
+      acc[v][e] = 0.f;
+      gy[v][e] = xv[v][e] = 0.f;
+    }
+  }
+  auto load_row = [&](int r, float (*g)[8], float (*xx)[8]) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = (v * blockDim.x + tid) * 8;
+      if (col_ok[v] && r < rows) {
+        ActT<T>::ld8(dy + (size_t)r * dim + c, g[v]);
+        ActT<T>::ld8(x + (size_t)r * dim + c, xx[v]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) g[v][e] = xx[v][e] = 0.f;
+      }
+    }
+  };
+  const float inv_dim = 1.0f / (float)dim;
+  int parity = 0;
+  int r = blockIdx.x;
+  if (r < rows) load_row(r, gy, xv);
+  for (; r < rows; r += gridDim.x) {
+    const float inv = 1.0f / rms[r];
+    float part = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) part = fmaf(gy[v][e] * sc[v][e], xv[v][e], part);
+    load_row(r + gridDim.x, gyn, xvn);  // next row in flight during the reduction
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) red[parity][warp] = part;
+    __syncthreads();
+    float dot = 0.f;
+    for (int i = 0; i < nw; ++i) dot += red[parity][i];
+    parity ^= 1;
+    const float k = dot * inv * inv * inv_dim;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = (v * blockDim.x + tid) * 8;
+      if (col_ok[v]) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          o[e] = inv * (sc[v][e] * gy[v][e]) - inv * (xv[v][e] * k);
+          acc[v][e] = fmaf(gy[v][e] * xv[v][e], inv, acc[v][e]);
+        }
+        ActT<float>::st8(dx + (size_t)r * dim + c, o);
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        gy[v][e] = gyn[v][e];
+        xv[v][e] = xvn[v][e];
+      }
+  }
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = (v * blockDim.x + tid) * 8;
+    if (col_ok[v]) ActT<float>::st8(ws + (size_t)blockIdx.x * dim + c, acc[v]);
+  }
+}
+
+__global__ void rms_reduce_kernel(const float* __restrict__ ws, float* dscale, int dim, int g) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= dim) return;
+  float a = 0.f;
+  for (int k = 0; k < g; ++k) a += ws[(size_t)k * dim + i];
+  dscale[i] += a;
+}
+
+struct RmsPlan {
+  int vpt, threads, grid;
+  size_t bytes;
+};
+
+inline RmsPlan rms_plan(int rows, int dim) {
+  RmsPlan p;
+  const int groups = dim / 8;
+  p.vpt = groups <= 1024 ? 1 : groups <= 2048 ? 2 : 4;
+  p.threads = ((groups + p.vpt - 1) / p.vpt + 31) / 32 * 32;
+  p.grid = rows < 1024 ? rows : 1024;
+  p.bytes = (size_t)p.grid * dim * sizeof(float);
+  return p;
+}
+
+int rms_validate(int rows, int dim, int dtype) {
+  if (rows <= 0 || dim <= 0) return SS_ERR_DIM;
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  if (dim % 8 != 0) return SS_ERR_ALIGN;
+  if (dim > kRmsMaxDim) return SS_ERR_DIM;
+  return SS_OK;
+}
+
+template <typename T>
+int rms_launch(const void* dy, const void* x, const float* scale, const float* rms, float* dx, float* dscale, int rows,
+               int dim, float* ws, const RmsPlan& pl, cudaStream_t s) {
+  const T* g = static_cast<const T*>(dy);
+  const T* xx = static_cast<const T*>(x);
+  if (pl.vpt == 1) rms_bwd_kernel<T, 1><<<pl.grid, pl.threads, 0, s>>>(g, xx, scale, rms, dx, ws, rows, dim);
+  else if (pl.vpt == 2) rms_bwd_kernel<T, 2><<<pl.grid, pl.threads, 0, s>>>(g, xx, scale, rms, dx, ws, rows, dim);
+  else rms_bwd_kernel<T, 4><<<pl.grid, pl.threads, 0, s>>>(g, xx, scale, rms, dx, ws, rows, dim);
+  if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+  rms_reduce_kernel<<<(dim + 255) / 256, 256, 0, s>>>(ws, dscale, dim, pl.grid);
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" size_t rmsnorm_bwd_workspace_size(int rows, int dim) {
+  if (rms_validate(rows, dim, SS_F32) != SS_OK) return 0;
+  return rms_plan(rows, dim).bytes;
+}
+
+extern "C" int rmsnorm_bwd(const void* dy, const void* x, const float* scale, const float* rms, float* dx, float* dscale,
+                           int rows, int dim, int dtype, void* workspace, size_t ws_bytes, void* stream) {
+  if (!dy || !x || !scale || !rms || !dx || !dscale) return SS_ERR_NULL;
+  const int v = rms_validate(rows, dim, dtype);
+  if (v != SS_OK) return v;
+  const void* ptrs[] = {dy, x, scale, rms, dx, dscale};
+  for (const void* q : ptrs)
+    if (!ssh::aligned16(q)) return SS_ERR_ALIGN;
+  const RmsPlan pl = rms_plan(rows, dim);
+  if (workspace == nullptr || ws_bytes < pl.bytes) return SS_ERR_WORKSPACE;
+  if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* ws = static_cast<float*>(workspace);
+  if (dtype == SS_F32) return rms_launch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+  return rms_launch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+}

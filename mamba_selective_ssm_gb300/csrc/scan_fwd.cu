@@ -1,0 +1,308 @@
+// Selective-scan forward (ss_scan_fwd) for sm_103a.
+//
+//   h_t = exp(delta_t * A) * h_{t-1} + delta_t * B_t * x_t,   y_t = (C_t . h_t + D x_t) * silu(z_t)
+//
+// One CTA = 64 channels of one batch row; the sequence is walked once, in
+// order, 16 steps per TMA tile, with the N-state recurrences of every channel
+// held in registers (2 channels x 4 states per thread, f32x2-packed).  The
+// exponent uses one ex2 per (t, d, n) with A pre-scaled by log2 e.  Per tile:
+//   1. thread 0 waits (bounded) on the tile's mbarrier;
+//   2. all threads widen delta, delta*x, B_t, C_t to fp32 in shared memory;
+//   3. every thread advances its 8 recurrences over the 16 steps and the NG
+//      lanes of a channel pair reduce C_t . h_t across states;
+//   4. the tile epilogue forms y = (s + D x) * silu(z) with 16-byte stores;
+//   5. thread 0 re-arms the freed stage with the tile NST ahead.
+// The state entering step c*chunk is stored as checkpoint c for the backward.
+#include "scan_common.cuh"
+
+namespace {
+
+using namespace ssk;
+
+__device__ unsigned g_fwd_err;
+
+constexpr int kNST = 4;  // TMA pipeline depth (tiles in flight)
+
+template <typename T, int N>
+struct FwdSmem {
+  alignas(128) T dlt[kNST][kTT * kDT];
+  alignas(128) T x[kNST][kTT * kDT];
+  alignas(128) T z[kNST][kTT * kDT];
+  alignas(128) T Bm[kNST][kTT * N];
+  alignas(128) T Cm[kNST][kTT * N];
+  alignas(16) float dlt_f[kTT * kDT];
+  alignas(16) float dx_f[kTT * kDT];
+  alignas(16) float B_f[kTT * N];
+  alignas(16) float C_f[kTT * N];
+  alignas(16) float s_f[kTT * kDT];
+  alignas(16) float Dv_s[kDT];
+  alignas(8) uint64_t full[kNST];
+};
+
+struct FwdParams {
+  const float* A;
+  const float* Dv;
+  const float* h0;
+  void* y;
+  float* ckpt;
+  float* h_last;
+  int B, L, D, chunk, nchunks;
+};
+
+template <int N, typename T>
+__global__ void __launch_bounds__(Geo<N>::NT) scan_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
+                                                              const __grid_constant__ CUtensorMap tm_x,
+                                                              const __grid_constant__ CUtensorMap tm_z,
+                                                              const __grid_constant__ CUtensorMap tm_B,
+                                                              const __grid_constant__ CUtensorMap tm_C) {
+  using G = Geo<N>;
+  using AT = ActT<T>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  FwdSmem<T, N>& S = *reinterpret_cast<FwdSmem<T, N>*>(smem_raw);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ng = lane % G::NG, cg = lane / G::NG;
+  const int dl = warp * G::WC + cg * 2;  // first of the thread's two channels, CTA-local
+  const int d0 = blockIdx.x * kDT;
+  const int dg = d0 + dl;
+  const bool dvalid = dg < p.D;  // D is a multiple of 8, so dg+1 < D as well
+  const int n0 = ng * 4;
+  const int L = p.L;
+  const int ntiles = (L + kTT - 1) / kTT;
+  const int nb = (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;  // batch rows of this CTA
+  const int nitems = nb * ntiles;
+  constexpr uint32_t kActBytes = kTT * kDT * AT::kBytes;
+  constexpr uint32_t kBCBytes = kTT * N * AT::kBytes;
+  constexpr uint32_t kStageBytes = 3 * kActBytes + 2 * kBCBytes;
+
+  // exponent scale A * log2(e) of the thread's 2 x 4 cells
+  float2 Ap[2][2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      if (dvalid) {
+        const float* a = p.A + (size_t)(dg + j) * N + n0 + 2 * q;
+        Ap[j][q] = f2(a[0] * kLog2e, a[1] * kLog2e);
+      } else {
+        Ap[j][q] = f2(0.f, 0.f);
+      }
+    }
+  for (int c = tid; c < kDT; c += G::NT) S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
+
+  auto issue = [&](int k) {
+    const int slot = k % kNST;
+    const int bb = (int)blockIdx.y + (k / ntiles) * (int)gridDim.y;
+    const int t0 = (k % ntiles) * kTT;
+    mbar_arrive_expect_tx(&S.full[slot], kStageBytes);
+    tma_load_3d(S.dlt[slot], &tm_dlt, &S.full[slot], d0, t0, bb);
+    tma_load_3d(S.x[slot], &tm_x, &S.full[slot], d0, t0, bb);
+    tma_load_3d(S.z[slot], &tm_z, &S.full[slot], d0, t0, bb);
+    tma_load_2d(S.Bm[slot], &tm_B, &S.full[slot], t0 * N, bb);
+    tma_load_2d(S.Cm[slot], &tm_C, &S.full[slot], t0 * N, bb);
+  };
+
+  if (tid == 0) {
+    prefetch_tmap(&tm_dlt); prefetch_tmap(&tm_x); prefetch_tmap(&tm_z); prefetch_tmap(&tm_B); prefetch_tmap(&tm_C);
+    for (int s = 0; s < kNST; ++s) mbar_init(&S.full[s], 1);
+    fence_barrier_init();
+    for (int k = 0; k < kNST && k < nitems; ++k) issue(k);
+  }
+  __syncthreads();
+
+  float2 h[2][2];
+  for (int k = 0; k < nitems; ++k) {
+    const int slot = k % kNST;
+    const int b = (int)blockIdx.y + (k / ntiles) * (int)gridDim.y;
+    const int ti = k % ntiles;
+    const int t0 = ti * kTT;
+
+    if (ti == 0) {  // entering batch row b: initial state
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.h0 != nullptr && dvalid) v = *reinterpret_cast<const float4*>(p.h0 + ((size_t)b * p.D + dg + j) * N + n0);
+        h[j][0] = f2(v.x, v.y);
+        h[j][1] = f2(v.z, v.w);
+      }
+    }
+
+    bool ok = true;
+    if (tid == 0) ok = mbar_wait_bounded(&S.full[slot], (k / kNST) & 1, kWaitLimitNs);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicOr(&g_fwd_err, kErrTmaTimeout);
+        for (int k2 = k; k2 < k + kNST && k2 < nitems; ++k2)
+          mbar_wait_bounded(&S.full[k2 % kNST], (k2 / kNST) & 1, 100000000ull);
+      }
+      return;
+    }
+
+    // widen the tile to fp32: delta, delta*x, B, C
+    for (int gi = tid; gi < kTT * kDT / 8; gi += G::NT) {
+      float dv[8], xv[8];
+      AT::ld8(&S.dlt[slot][gi * 8], dv);
+      AT::ld8(&S.x[slot][gi * 8], xv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xv[e] *= dv[e];
+      float4* dst = reinterpret_cast<float4*>(&S.dlt_f[gi * 8]);
+      dst[0] = make_float4(dv[0], dv[1], dv[2], dv[3]);
+      dst[1] = make_float4(dv[4], dv[5], dv[6], dv[7]);
+      float4* dst2 = reinterpret_cast<float4*>(&S.dx_f[gi * 8]);
+      dst2[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
+      dst2[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+    }
+    for (int gi = tid; gi < kTT * N / 4; gi += G::NT) {
+      float bv[4], cv[4];
+      AT::ld4(&S.Bm[slot][gi * 4], bv);
+      AT::ld4(&S.Cm[slot][gi * 4], cv);
+      reinterpret_cast<float4*>(S.B_f)[gi] = make_float4(bv[0], bv[1], bv[2], bv[3]);
+      reinterpret_cast<float4*>(S.C_f)[gi] = make_float4(cv[0], cv[1], cv[2], cv[3]);
+    }
+    __syncthreads();
+
+    // checkpoint: the state entering step t0 (chunk is a multiple of the tile)
+    if (dvalid && (t0 % p.chunk) == 0) {
+      const int c = t0 / p.chunk;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        *reinterpret_cast<float4*>(p.ckpt + (((size_t)b * p.D + dg + j) * p.nchunks + c) * N + n0) =
+            make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
+    }
+
+    // the recurrence over the tile's 16 steps (steps past L were zero-filled
+    // by TMA: delta = 0 gives a = 1 and no input, so they leave h unchanged)
+#pragma unroll 4
+    for (int r = 0; r < kTT; ++r) {
+      const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[r * kDT + dl]);
+      const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * kDT + dl]);
+      const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
+      const float4 Cv = *reinterpret_cast<const float4*>(&S.C_f[r * N + n0]);
+      const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
+      const float2 C01 = f2(Cv.x, Cv.y), C23 = f2(Cv.z, Cv.w);
+      float yj[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float2 dj = bc2(j ? dd.y : dd.x);
+        const float2 xj = bc2(j ? xx.y : xx.x);
+        const float2 a0 = ex2_2(mul2(dj, Ap[j][0]));
+        const float2 a1 = ex2_2(mul2(dj, Ap[j][1]));
+        h[j][0] = fma2(a0, h[j][0], mul2(xj, B01));
+        h[j][1] = fma2(a1, h[j][1], mul2(xj, B23));
+        const float2 yy = fma2(C23, h[j][1], mul2(C01, h[j][0]));
+        yj[j] = yy.x + yy.y;
+      }
+      // C_t . h_t across the NG lanes of the pair group
+      if constexpr (G::NG == 4) {
+        const bool up = ng & 2;
+        float keep = up ? yj[1] : yj[0];
+        keep += __shfl_xor_sync(0xffffffffu, up ? yj[0] : yj[1], 2);
+        keep += __shfl_xor_sync(0xffffffffu, keep, 1);
+        if ((ng & 1) == 0) S.s_f[r * kDT + dl + (ng >> 1)] = keep;
+      } else if constexpr (G::NG == 2) {
+        const bool up = ng & 1;
+        float keep = up ? yj[1] : yj[0];
+        keep += __shfl_xor_sync(0xffffffffu, up ? yj[0] : yj[1], 1);
+        S.s_f[r * kDT + dl + ng] = keep;
+      } else {
+        *reinterpret_cast<float2*>(&S.s_f[r * kDT + dl]) = f2(yj[0], yj[1]);
+      }
+    }
+    __syncthreads();
+
+    // epilogue: y = (s + D x) * silu(z)
+    for (int gi = tid; gi < kTT * kDT / 8; gi += G::NT) {
+      const int r = gi / (kDT / 8), c8 = (gi % (kDT / 8)) * 8;
+      const int t = t0 + r, d = d0 + c8;
+      if (t < L && d < p.D) {
+        float xv[8], zv[8], o[8];
+        AT::ld8(&S.x[slot][r * kDT + c8], xv);
+        AT::ld8(&S.z[slot][r * kDT + c8], zv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float s = S.s_f[r * kDT + c8 + e] + S.Dv_s[c8 + e] * xv[e];
+          o[e] = s * zv[e] * sigmoid(zv[e]);
+        }
+        AT::st8(reinterpret_cast<T*>(p.y) + ((size_t)b * L + t) * p.D + d, o);
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && k + kNST < nitems) issue(k + kNST);
+
+    if (ti == ntiles - 1 && p.h_last != nullptr && dvalid) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        *reinterpret_cast<float4*>(p.h_last + ((size_t)b * p.D + dg + j) * N + n0) =
+            make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
+    }
+  }
+}
+
+template <int N, typename T>
+int launch_fwd(const FwdParams& p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z,
+               cudaStream_t stream) {
+  constexpr int e = ActT<T>::kBytes;
+  CUtensorMap tm[5];
+  const uint64_t adims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
+  const uint64_t astr[2] = {(uint64_t)p.D * e, (uint64_t)p.L * p.D * e};
+  const uint32_t abox[3] = {kDT, kTT, 1};
+  const uint64_t bdims[2] = {(uint64_t)p.L * N, (uint64_t)p.B};
+  const uint64_t bstr[1] = {(uint64_t)p.L * N * e};
+  const uint32_t bbox[2] = {kTT * N, 1};
+  if (!ssh::encode_tiled(&tm[0], ActT<T>::kTma, 3, delta, adims, astr, abox) ||
+      !ssh::encode_tiled(&tm[1], ActT<T>::kTma, 3, x, adims, astr, abox) ||
+      !ssh::encode_tiled(&tm[2], ActT<T>::kTma, 3, z, adims, astr, abox) ||
+      !ssh::encode_tiled(&tm[3], ActT<T>::kTma, 2, Bm, bdims, bstr, bbox) ||
+      !ssh::encode_tiled(&tm[4], ActT<T>::kTma, 2, Cm, bdims, bstr, bbox))
+    return SS_ERR_CUDA;
+  const int ndt = (p.D + kDT - 1) / kDT;
+  const int cap = 1024 / ndt > 0 ? 1024 / ndt : 1;  // about 1024 CTAs; each loops over its batch rows
+  const int gy = p.B < cap ? p.B : cap;
+  const size_t smem = sizeof(FwdSmem<T, N>);
+  auto kern = scan_fwd_kernel<N, T>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
+  kern<<<dim3(ndt, gy), Geo<N>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace ssh {
+int read_clear_fwd_err(cudaStream_t s, unsigned* out) {
+  unsigned zero = 0;
+  if (cudaMemcpyFromSymbolAsync(out, g_fwd_err, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SS_ERR_CUDA;
+  if (cudaMemcpyToSymbolAsync(g_fwd_err, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, s) != cudaSuccess) return SS_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+}  // namespace ssh
+
+extern "C" int ss_scan_num_chunks(int L, int chunk) { return (L > 0 && chunk > 0) ? (L + chunk - 1) / chunk : 0; }
+
+extern "C" int ss_scan_fwd(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm, const float* Dv,
+                           const void* z, const float* h0, void* y, float* ckpt, float* h_last, int B, int L, int D, int N,
+                           int chunk, int dtype, void* stream) {
+  if (!x || !delta || !A || !Bm || !Cm || !Dv || !z || !y || !ckpt) return SS_ERR_NULL;
+  if (B <= 0 || L <= 0 || D <= 0 || N <= 0 || chunk <= 0) return SS_ERR_DIM;
+  if (N != 4 && N != 8 && N != 16) return SS_ERR_UNSUPPORTED;
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  if (chunk % kTT != 0) return SS_ERR_UNSUPPORTED;
+  if (D % 8 != 0) return SS_ERR_ALIGN;
+  // the B_t / C_t rows of one batch element must span a multiple of 16 bytes (TMA stride rule)
+  if (((long long)L * N * (dtype == SS_F32 ? 4 : 2)) % 16 != 0) return SS_ERR_ALIGN;
+  const void* ptrs[] = {x, delta, A, Bm, Cm, Dv, z, y, ckpt};
+  for (const void* q : ptrs)
+    if (!ssh::aligned16(q)) return SS_ERR_ALIGN;
+  if ((h0 && !ssh::aligned16(h0)) || (h_last && !ssh::aligned16(h_last))) return SS_ERR_ALIGN;
+  // TMA coordinates and tensor extents are 32-bit
+  if ((long long)L * N >= (1ll << 31) || (long long)L * D >= (1ll << 40)) return SS_ERR_DIM;
+  FwdParams p{A, Dv, h0, y, ckpt, h_last, B, L, D, chunk, ss_scan_num_chunks(L, chunk)};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == SS_F32) {
+    if (N == 4) return launch_fwd<4, float>(p, x, delta, Bm, Cm, z, s);
+    if (N == 8) return launch_fwd<8, float>(p, x, delta, Bm, Cm, z, s);
+    return launch_fwd<16, float>(p, x, delta, Bm, Cm, z, s);
+  }
+  if (N == 4) return launch_fwd<4, __nv_bfloat16>(p, x, delta, Bm, Cm, z, s);
+  if (N == 8) return launch_fwd<8, __nv_bfloat16>(p, x, delta, Bm, Cm, z, s);
+  return launch_fwd<16, __nv_bfloat16>(p, x, delta, Bm, Cm, z, s);
+}

@@ -1,0 +1,174 @@
+"""PyTorch-facing calls of libssscan: argument checks, output allocation and the
+C-ABI call on the current CUDA stream.  No arithmetic of the method is done here.
+
+Names and argument order follow include/ssscan.h:
+
+* ``ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk=64)``
+  -> ``(y, ckpt, h_last)``
+* ``ss_scan_bwd(x, delta, A, Bm, Cm, Dv, z, ckpt, dy, dh_last=None, chunk=64, dA=None, dD=None, ...)``
+  -> dict of gradients
+* ``conv1d_causal_bwd(dout, x, w, dw=None, db=None)`` -> ``(dx, dw, db)``
+* ``rmsnorm_bwd(dy, x, scale, rms, dscale=None)`` -> ``(dx, dscale)``
+
+Activations are ``torch.float32`` or ``torch.bfloat16`` CUDA tensors, contiguous;
+parameters, states and gradients are ``torch.float32``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _capi
+from ._capi import SS_BF16, SS_F32, check, load
+
+_DT = {torch.float32: SS_F32, torch.bfloat16: SS_BF16}
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _req(t, name, shape=None, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (strided views are not accepted)")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def _act_dtype(x):
+    if x.dtype not in _DT:
+        raise ValueError(f"activations must be float32 or bfloat16, got {x.dtype}")
+    return _DT[x.dtype]
+
+
+def num_chunks(L: int, chunk: int) -> int:
+    return load().ss_scan_num_chunks(L, chunk)
+
+
+def ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int = 64, want_h_last: bool = True):
+    lib = load()
+    B, L, D = x.shape
+    N = A.shape[1]
+    dev, dt = x.device, x.dtype
+    _act_dtype(x)
+    for name, t in (("x", x), ("delta", delta), ("z", z)):
+        _req(t, name, (B, L, D), dt, dev)
+    for name, t in (("Bm", Bm), ("Cm", Cm)):
+        _req(t, name, (B, L, N), dt, dev)
+    _req(A, "A", (D, N), torch.float32, dev)
+    _req(Dv, "Dv", (D,), torch.float32, dev)
+    if h0 is not None:
+        _req(h0, "h0", (B, D, N), torch.float32, dev)
+    nck = num_chunks(L, chunk) if L > 0 and chunk > 0 else 0
+    y = torch.empty_like(x)
+    ckpt = torch.empty((B, D, max(nck, 1), N), device=dev, dtype=torch.float32)
+    h_last = torch.empty((B, D, N), device=dev, dtype=torch.float32) if want_h_last else None
+    rc = lib.ss_scan_fwd(_p(x), _p(delta), _p(A), _p(Bm), _p(Cm), _p(Dv), _p(z), _p(h0), _p(y), _p(ckpt), _p(h_last),
+                         B, L, D, N, chunk, _DT[dt], _stream())
+    check(rc, "ss_scan_fwd")
+    return y, ckpt, h_last
+
+
+def scan_bwd_workspace_size(B, L, D, N, chunk, dtype) -> int:
+    return load().ss_scan_bwd_workspace_size(B, L, D, N, chunk, _DT[dtype])
+
+
+def ss_scan_bwd(x, delta, A, Bm, Cm, Dv, z, ckpt, dy, dh_last=None, chunk: int = 64, dA=None, dD=None,
+                want_dh0: bool = True, workspace=None, out=None):
+    """Gradients of sum(y*dy) (+ sum(h_last*dh_last)).  dA and dD accumulate into the
+    given tensors (zeros when None); the rest are returned freshly (or written into ``out``)."""
+    lib = load()
+    B, L, D = x.shape
+    N = A.shape[1]
+    dev, dt = x.device, x.dtype
+    _act_dtype(x)
+    for name, t in (("x", x), ("delta", delta), ("z", z), ("dy", dy)):
+        _req(t, name, (B, L, D), dt, dev)
+    for name, t in (("Bm", Bm), ("Cm", Cm)):
+        _req(t, name, (B, L, N), dt, dev)
+    _req(A, "A", (D, N), torch.float32, dev)
+    _req(Dv, "Dv", (D,), torch.float32, dev)
+    _req(ckpt, "ckpt", (B, D, num_chunks(L, chunk), N), torch.float32, dev)
+    if dh_last is not None:
+        _req(dh_last, "dh_last", (B, D, N), torch.float32, dev)
+    f32 = dict(device=dev, dtype=torch.float32)
+    if out is None:
+        out = {
+            "dx": torch.empty((B, L, D), **f32), "ddelta": torch.empty((B, L, D), **f32),
+            "dz": torch.empty((B, L, D), **f32), "dB": torch.empty((B, L, N), **f32),
+            "dC": torch.empty((B, L, N), **f32),
+            "dh0": torch.empty((B, D, N), **f32) if want_dh0 else None,
+        }
+    out["dA"] = torch.zeros((D, N), **f32) if dA is None else _req(dA, "dA", (D, N), torch.float32, dev)
+    out["dD"] = torch.zeros((D,), **f32) if dD is None else _req(dD, "dD", (D,), torch.float32, dev)
+    ws_bytes = lib.ss_scan_bwd_workspace_size(B, L, D, N, chunk, _DT[dt])
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), device=dev, dtype=torch.uint8)
+    rc = lib.ss_scan_bwd(_p(x), _p(delta), _p(A), _p(Bm), _p(Cm), _p(Dv), _p(z), _p(ckpt), _p(dy), _p(dh_last),
+                         _p(out["dx"]), _p(out["ddelta"]), _p(out["dz"]), _p(out["dA"]), _p(out["dB"]), _p(out["dC"]),
+                         _p(out["dD"]), _p(out.get("dh0")), B, L, D, N, chunk, _DT[dt], _p(workspace),
+                         workspace.numel() * workspace.element_size(), _stream())
+    check(rc, "ss_scan_bwd")
+    return out
+
+
+def conv1d_causal_bwd(dout, x, w, dw=None, db=None, workspace=None):
+    lib = load()
+    B, L, D = x.shape
+    K = w.shape[1]
+    dev = x.device
+    xdt = _act_dtype(x)
+    _req(dout, "dout", (B, L, D), torch.float32, dev)
+    _req(x, "x", (B, L, D), x.dtype, dev)
+    _req(w, "w", (D, K), torch.float32, dev)
+    dw = torch.zeros((D, K), device=dev, dtype=torch.float32) if dw is None else _req(dw, "dw", (D, K), torch.float32, dev)
+    db = torch.zeros((D,), device=dev, dtype=torch.float32) if db is None else _req(db, "db", (D,), torch.float32, dev)
+    dx = torch.empty((B, L, D), device=dev, dtype=torch.float32)
+    ws_bytes = lib.conv1d_causal_bwd_workspace_size(B, L, D, K)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), device=dev, dtype=torch.uint8)
+    rc = lib.conv1d_causal_bwd(_p(dout), _p(x), _p(w), _p(dx), _p(dw), _p(db), B, L, D, K, xdt, _p(workspace),
+                               workspace.numel() * workspace.element_size(), _stream())
+    check(rc, "conv1d_causal_bwd")
+    return dx, dw, db
+
+
+def rmsnorm_bwd(dy, x, scale, rms, dscale=None, workspace=None):
+    lib = load()
+    R, H = x.shape
+    dev = x.device
+    dt = _act_dtype(x)
+    _req(dy, "dy", (R, H), x.dtype, dev)
+    _req(x, "x", (R, H), x.dtype, dev)
+    _req(scale, "scale", (H,), torch.float32, dev)
+    _req(rms, "rms", (R,), torch.float32, dev)
+    dscale = torch.zeros((H,), device=dev, dtype=torch.float32) if dscale is None else _req(
+        dscale, "dscale", (H,), torch.float32, dev)
+    dx = torch.empty((R, H), device=dev, dtype=torch.float32)
+    ws_bytes = lib.rmsnorm_bwd_workspace_size(R, H)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), device=dev, dtype=torch.uint8)
+    rc = lib.rmsnorm_bwd(_p(dy), _p(x), _p(scale), _p(rms), _p(dx), _p(dscale), R, H, dt, _p(workspace),
+                         workspace.numel() * workspace.element_size(), _stream())
+    check(rc, "rmsnorm_bwd")
+    return dx, dscale
+
+
+def device_status() -> int:
+    """Reads and clears the library's device error word (synchronises the current stream)."""
+    return load().ss_device_status(_stream())

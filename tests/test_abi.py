@@ -1,0 +1,136 @@
+"""The C ABI on the host: the library builds and loads, exports every symbol that
+include/ssscan.h declares, and rejects bad arguments with the documented
+status codes before touching the GPU (CPU only; no kernel is launched)."""
+
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssscan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from mamba_selective_ssm_gb300 import _build, _capi
+    _build.build()
+    return _capi.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)) - {"defined"})
+
+
+def test_header_declares_the_four_entry_points():
+    names = _declared_functions()
+    for n in ("ss_scan_fwd", "ss_scan_bwd", "conv1d_causal_bwd", "rmsnorm_bwd", "ss_strerror"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from mamba_selective_ssm_gb300._capi import SIGNATURES
+    names = _declared_functions()
+    assert set(names) == set(SIGNATURES), (names, sorted(SIGNATURES))
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_covers_codes(lib):
+    for c in range(-7, 1):
+        assert lib.ss_strerror(c) and b"unknown" not in lib.ss_strerror(c)
+    assert b"unknown" in lib.ss_strerror(-99)
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def test_scan_fwd_validation(lib):
+    from mamba_selective_ssm_gb300 import _capi as c
+    p = [_fake(0x10000 + 256 * i) for i in range(11)]
+
+    def call(ptrs=p, B=2, L=64, D=16, N=4, chunk=64, dtype=c.SS_F32):
+        return lib.ss_scan_fwd(*ptrs, B, L, D, N, chunk, dtype, None)
+
+    q = list(p)
+    q[0] = None
+    assert call(q) == c.SS_ERR_NULL
+    q = list(p)
+    q[7] = None  # h0 optional -> only later checks fail
+    assert call(q, B=0) == c.SS_ERR_DIM
+    assert call(B=0) == c.SS_ERR_DIM
+    assert call(L=-1) == c.SS_ERR_DIM
+    assert call(chunk=0) == c.SS_ERR_DIM
+    assert call(N=5) == c.SS_ERR_UNSUPPORTED
+    assert call(N=32) == c.SS_ERR_UNSUPPORTED
+    assert call(dtype=7) == c.SS_ERR_UNSUPPORTED
+    assert call(chunk=24) == c.SS_ERR_UNSUPPORTED
+    assert call(D=12) == c.SS_ERR_ALIGN
+    assert call(L=63, N=4, dtype=c.SS_BF16) == c.SS_ERR_ALIGN  # B_t rows of 8*63 bytes
+    q = list(p)
+    q[3] = _fake(0x10004)
+    assert call(q) == c.SS_ERR_ALIGN
+
+
+def test_scan_bwd_validation_and_workspace(lib):
+    from mamba_selective_ssm_gb300 import _capi as c
+    ws = lib.ss_scan_bwd_workspace_size(2, 64, 16, 4, 64, c.SS_F32)
+    assert ws > 0
+    # dB/dC partials per 64-channel tile + dA/dD partials per CTA row
+    assert ws >= 1 * 2 * 64 * 2 * 4 * 4 + 2 * 16 * 4 * 4 + 2 * 16 * 4
+    assert lib.ss_scan_bwd_workspace_size(0, 64, 16, 4, 64, 0) == 0
+    assert lib.ss_scan_bwd_workspace_size(2, 64, 16, 4, 4096, 0) == 0  # window states exceed shared memory
+    p = [_fake(0x10000 + 256 * i) for i in range(18)]
+
+    def call(ptrs=p, B=2, L=64, D=16, N=4, chunk=64, dtype=c.SS_F32, w=_fake(0x90000), wsz=ws):
+        return lib.ss_scan_bwd(*ptrs, B, L, D, N, chunk, dtype, w, wsz, None)
+
+    q = list(p)
+    q[8] = None  # dy
+    assert call(q) == c.SS_ERR_NULL
+    assert call(N=3) == c.SS_ERR_UNSUPPORTED
+    assert call(D=20) == c.SS_ERR_ALIGN
+    assert call(w=None) == c.SS_ERR_WORKSPACE
+    assert call(wsz=ws - 1) == c.SS_ERR_WORKSPACE
+    assert call(w=_fake(0x90008)) == c.SS_ERR_ALIGN
+
+
+def test_conv_and_rms_validation(lib):
+    from mamba_selective_ssm_gb300 import _capi as c
+    assert lib.conv1d_causal_bwd_workspace_size(4, 2048, 4096, 4) > 0
+    assert lib.conv1d_causal_bwd_workspace_size(4, 2048, 4096, 5) == 0
+    p = [_fake(0x10000 + 256 * i) for i in range(6)]
+    ws = lib.conv1d_causal_bwd_workspace_size(2, 10, 16, 4)
+    assert lib.conv1d_causal_bwd(*p, 2, 10, 16, 5, c.SS_F32, _fake(0x90000), ws, None) == c.SS_ERR_UNSUPPORTED
+    assert lib.conv1d_causal_bwd(*p, 2, 10, 16, 4, 3, _fake(0x90000), ws, None) == c.SS_ERR_UNSUPPORTED
+    assert lib.conv1d_causal_bwd(*p, 2, 10, 12, 4, c.SS_F32, _fake(0x90000), ws, None) == c.SS_ERR_ALIGN
+    assert lib.conv1d_causal_bwd(*p, 2, 10, 16, 4, c.SS_F32, None, ws, None) == c.SS_ERR_WORKSPACE
+    assert lib.conv1d_causal_bwd(None, *p[1:], 2, 10, 16, 4, c.SS_F32, _fake(0x90000), ws, None) == c.SS_ERR_NULL
+    wr = lib.rmsnorm_bwd_workspace_size(100, 768)
+    assert wr == 100 * 768 * 4
+    assert lib.rmsnorm_bwd_workspace_size(10, 65536) == 0
+    assert lib.rmsnorm_bwd(*p, 100, 770, c.SS_F32, _fake(0x90000), wr, None) == c.SS_ERR_ALIGN
+    assert lib.rmsnorm_bwd(*p, 0, 768, c.SS_F32, _fake(0x90000), wr, None) == c.SS_ERR_DIM
+    assert lib.rmsnorm_bwd(*p, 100, 768, c.SS_F32, _fake(0x90000), wr - 4, None) == c.SS_ERR_WORKSPACE
+
+
+def test_num_chunks(lib):
+    assert lib.ss_scan_num_chunks(64, 64) == 1
+    assert lib.ss_scan_num_chunks(65, 64) == 2
+    assert lib.ss_scan_num_chunks(16384, 256) == 64
+    assert lib.ss_scan_num_chunks(0, 16) == 0
+
+
+def test_wrapper_rejects_strided_and_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    from mamba_selective_ssm_gb300 import ops
+    t = torch.zeros(4, 4)
+    with pytest.raises(ValueError, match="CUDA"):
+        ops._req(t, "x")
