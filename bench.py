@@ -1,0 +1,440 @@
+"""Throughput of the selective-scan hot path on GB300.
+
+One step = the whole path over one batch of synthetic Mamba-1.4B-shaped input
+(B=4, L=2048, d_model=2048, d_inner=4096, N=16, d_conv=4; bf16 activations,
+fp32 state and gradients), all inputs resident in HBM:
+    ss_scan_fwd -> ss_scan_bwd -> conv1d_causal_bwd ([B, L, 4096]) -> rmsnorm_bwd ([B*L, 2048])
+value = B*L*D elements per step / step time, summed over ranks (each rank runs
+its own replica: the path has no cross-GPU exchange at this size).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+Prints one JSON line (rank 0).
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "scan fwd+bwd (B·L·D)/s and achieved HBM GB/s vs GB300 peak, 1 GPU"
+UNIT = "(B*L*D)/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mamba1p4b")
+    ap.add_argument("--chunk", type=int, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- accounting
+
+def algorithmic_bytes(wl, chunk):
+    """Bytes each call must move (scratch excluded): reads of its inputs, writes of its outputs."""
+    e = 2 if wl.dtype == "bf16" else 4
+    B, L, D, N, K, H = wl.B, wl.L, wl.D, wl.N, wl.d_conv, wl.d_model
+    E = B * L * D
+    nck = -(-L // chunk)
+    ck = B * D * nck * N * 4
+    small = (D * N + D) * 4
+    return {
+        "scan_fwd": E * 4 * e + B * L * N * 2 * e + ck + small,
+        "scan_bwd": E * (4 * e + 12) + B * L * N * (2 * e + 8) + ck + 3 * small,
+        "conv1d_bwd": E * (4 + e + 4) + D * (K + 1) * 4 * 3,
+        "rmsnorm_bwd": B * L * H * (2 * e + 4) + B * L * 4 + 3 * H * 4,
+    }
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(name):
+    f = {"scan_bwd": "scan_bwd.cu", "scan_fwd": "scan_fwd.cu", "conv1d_bwd": "conv1d_bwd.cu",
+         "rmsnorm_bwd": "rmsnorm_bwd.cu"}[name]
+    h = hashlib.sha256()
+    for part in (f, "scan_common.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "mamba_selective_ssm_gb300", "csrc", part), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name, wl_name):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)[f"{name}:{wl_name}"]
+    except Exception:
+        return None
+    return rec["bytes_per_launch"] if rec.get("source_hash") == kernel_source_hash(name) else None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (timestamped) of SM clock and throttle reasons; keeps those inside [t0, t1]."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20"]
+        if bus_id:
+            cmd.insert(1, f"--id={bus_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for (ts, s) in self.samples if t0 - 0.03 <= ts <= t1 + 0.03]
+        if not inside:
+            inside = [s for (_, s) in self.samples[-3:]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in inside for n, v in zip(names, s[4:8]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_init(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws, device=None):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle (CPU baseline / reference arm)
+
+def oracle_sample(wl, d_sample, seed=0):
+    """The float64 oracle on one batch row and the first d_sample channels of the workload."""
+    import numpy as np
+    from oracle import conv1d_causal_bwd_ref, rmsnorm_bwd_ref, scan_bwd_ref, scan_fwd_ref
+    from workloads import make_conv_inputs, make_rmsnorm_inputs, make_scan_inputs
+    sw = wl.with_(B=1, D=d_sample, d_model=max(8, d_sample // 2))
+    inp = make_scan_inputs(sw, seed)
+    cv = make_conv_inputs(sw, seed)
+    rm = make_rmsnorm_inputs(sw, seed)
+    args = (inp["x"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], inp["Dv"], inp["z"])
+
+    def run():
+        scan_fwd_ref(*args, chunk=wl.chunk)
+        scan_bwd_ref(*args, inp["dy"])
+        conv1d_causal_bwd_ref(cv["dout"], cv["x"], cv["w"])
+        rmsnorm_bwd_ref(rm["dy"], rm["x"], rm["scale"], rm["rms"])
+
+    return run, sw.B * sw.L * sw.D, f"B=1, L={sw.L}, D={d_sample}, N={sw.N} of the {wl.name} layer (scan fwd+bwd, " \
+                                    f"conv1d bwd, RMSNorm bwd [L, {sw.d_model}]), float64 NumPy"
+
+
+def cpu_baseline(wl, d_sample=2048):
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    run, elems, desc = oracle_sample(wl, d_sample)
+    t = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t
+    return {"value": elems / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc, "seconds": round(dt, 3)}
+
+
+def run_reference(args, ws, rank):
+    from workloads import get_config
+    wl = get_config(args.workload)
+    if args.chunk:
+        wl = wl.with_(chunk=args.chunk)
+    if rank != 0:
+        return
+    d_sample = 64
+    run, elems, desc = oracle_sample(wl, d_sample)
+    for _ in range(args.warmup):
+        run()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t
+    v = elems * args.steps / dt
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "L": wl.L, "D": wl.D, "N": wl.N, "d_conv": wl.d_conv,
+                   "d_model": wl.d_model, "chunk": wl.chunk, "sample": desc},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        return
+    ws, rank, local = dist_init(args)
+    import numpy as np
+    import torch
+
+    import mamba_selective_ssm_gb300 as ss
+    from mamba_selective_ssm_gb300 import _capi
+    from workloads import get_config, make_conv_inputs, make_rmsnorm_inputs, make_scan_inputs
+
+    ss.build()
+    lib = ss.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = get_config(args.workload)
+    if args.chunk:
+        wl = wl.with_(chunk=args.chunk)
+    chunk = wl.chunk
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    sdt = _capi.SS_BF16 if wl.dtype == "bf16" else _capi.SS_F32
+    B, L, D, N, K, H = wl.B, wl.L, wl.D, wl.N, wl.d_conv, wl.d_model
+
+    # ---- inputs (seeded, synthetic; host copies kept pinned for the end-to-end leg)
+    inp = make_scan_inputs(wl, seed=rank)
+    cv = make_conv_inputs(wl, seed=rank)
+    rm = make_rmsnorm_inputs(wl, seed=rank)
+
+    def host_t(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dt).pin_memory()
+
+    H_in = {
+        "x": host_t(inp["x"], tdt), "delta": host_t(inp["delta"], tdt), "z": host_t(inp["z"], tdt),
+        "Bm": host_t(inp["Bm"], tdt), "Cm": host_t(inp["Cm"], tdt), "dy": host_t(inp["dy"], tdt),
+        "A": host_t(inp["A"], torch.float32), "Dv": host_t(inp["Dv"], torch.float32),
+        "c_dout": host_t(cv["dout"], torch.float32), "c_x": host_t(cv["x"], tdt), "c_w": host_t(cv["w"], torch.float32),
+        "r_dy": host_t(rm["dy"], tdt), "r_x": host_t(rm["x"], tdt), "r_scale": host_t(rm["scale"], torch.float32),
+        "r_rms": host_t(rm["rms"], torch.float32),
+    }
+    del inp, cv, rm
+    X = {k: v.to(dev) for k, v in H_in.items()}
+    f32 = dict(device=dev, dtype=torch.float32)
+    nck = lib.ss_scan_num_chunks(L, chunk)
+    O = {
+        "y": torch.empty((B, L, D), device=dev, dtype=tdt), "ckpt": torch.empty((B, nck, D, N), **f32),
+        "h_last": torch.empty((B, D, N), **f32),
+        "dx": torch.empty((B, L, D), **f32), "ddelta": torch.empty((B, L, D), **f32), "dz": torch.empty((B, L, D), **f32),
+        "dB": torch.empty((B, L, N), **f32), "dC": torch.empty((B, L, N), **f32), "dh0": torch.empty((B, D, N), **f32),
+        "dA": torch.zeros((D, N), **f32), "dD": torch.zeros((D,), **f32),
+        "c_dx": torch.empty((B, L, D), **f32), "c_dw": torch.zeros((D, K), **f32), "c_db": torch.zeros((D,), **f32),
+        "r_dx": torch.empty((B * L, H), **f32), "r_dscale": torch.zeros((H,), **f32),
+    }
+    ws_scan = lib.ss_scan_bwd_workspace_size(B, L, D, N, chunk, sdt)
+    ws_conv = lib.conv1d_causal_bwd_workspace_size(B, L, D, K)
+    ws_rms = lib.rmsnorm_bwd_workspace_size(B * L, H)
+    W = torch.empty(max(ws_scan, ws_conv, ws_rms), device=dev, dtype=torch.uint8)
+    p = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    wsz = W.numel()
+
+    calls = {
+        "scan_fwd": lambda: lib.ss_scan_fwd(p(X["x"]), p(X["delta"]), p(X["A"]), p(X["Bm"]), p(X["Cm"]), p(X["Dv"]),
+                                            p(X["z"]), None, p(O["y"]), p(O["ckpt"]), p(O["h_last"]),
+                                            B, L, D, N, chunk, sdt, sp),
+        "scan_bwd": lambda: lib.ss_scan_bwd(p(X["x"]), p(X["delta"]), p(X["A"]), p(X["Bm"]), p(X["Cm"]), p(X["Dv"]),
+                                            p(X["z"]), p(O["ckpt"]), p(X["dy"]), None, p(O["dx"]), p(O["ddelta"]),
+                                            p(O["dz"]), p(O["dA"]), p(O["dB"]), p(O["dC"]), p(O["dD"]), p(O["dh0"]),
+                                            B, L, D, N, chunk, sdt, p(W), wsz, sp),
+        "conv1d_bwd": lambda: lib.conv1d_causal_bwd(p(X["c_dout"]), p(X["c_x"]), p(X["c_w"]), p(O["c_dx"]),
+                                                    p(O["c_dw"]), p(O["c_db"]), B, L, D, K, sdt, p(W), wsz, sp),
+        "rmsnorm_bwd": lambda: lib.rmsnorm_bwd(p(X["r_dy"]), p(X["r_x"]), p(X["r_scale"]), p(X["r_rms"]),
+                                               p(O["r_dx"]), p(O["r_dscale"]), B * L, H, sdt, p(W), wsz, sp),
+    }
+    launches_per_step = 1 + 3 + 2 + 2  # fwd; bwd + dB/dC sum + dA/dD sum; conv + sum; rms + sum
+    names = list(calls)
+
+    def step(ev=None):
+        for i, n in enumerate(names):
+            if ev is not None:
+                ev[i][0].record(stream)
+            rc = calls[n]()
+            if rc != 0:
+                raise RuntimeError(f"{n}: {_capi.strerror(rc)}")
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    sampler = ClockSampler(bus) if rank == 0 else None
+    time.sleep(0.15)
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in names] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    barrier(ws)
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_total, ws, dev)
+    per_call = {n: sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps)) / args.steps
+                for i, n in enumerate(names)}
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+    if _capi.load().ss_device_status(sp) != 0:
+        raise RuntimeError("a kernel reported a device-side wait timeout")
+
+    ms_step = ms_total / args.steps
+    elems = B * L * D
+    value = elems * ws / (ms_step * 1e-3)
+    alg = algorithmic_bytes(wl, chunk)
+    peak, peak_kind = measured_peak()
+    kern = {}
+    for n in names:
+        gbs = alg[n] / (per_call[n] * 1e-3) / 1e9
+        kern[n] = {"ms": round(per_call[n], 5), "alg_bytes": alg[n], "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    dom = max(names, key=lambda n: per_call[n])
+    traffic = profiled_traffic(dom, wl.name)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["GB/s"], "peak": peak, "unit": "GB/s",
+                "frac": kern[dom]["frac"], "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                "alg_bytes_per_launch": alg[dom]}
+    scan_ms = per_call["scan_fwd"] + per_call["scan_bwd"]
+    scan_bytes = alg["scan_fwd"] + alg["scan_bwd"]
+
+    # ---- end to end through the public API: pinned host inputs in, results out, every step
+    e2e = None
+    if not args.no_e2e:
+        keys_in = list(H_in)
+        h2d = sum(H_in[k].numel() * H_in[k].element_size() for k in keys_in)
+        outs_host = {}
+
+        def e2e_step():
+            Xd = {k: H_in[k].to(dev, non_blocking=True) for k in keys_in}
+            y, ck, hl = ss.ss_scan_fwd(Xd["x"], Xd["delta"], Xd["A"], Xd["Bm"], Xd["Cm"], Xd["Dv"], Xd["z"], chunk=chunk)
+            g = ss.ss_scan_bwd(Xd["x"], Xd["delta"], Xd["A"], Xd["Bm"], Xd["Cm"], Xd["Dv"], Xd["z"], ck, Xd["dy"],
+                               chunk=chunk)
+            cdx, cdw, cdb = ss.conv1d_causal_bwd(Xd["c_dout"], Xd["c_x"], Xd["c_w"])
+            rdx, rds = ss.rmsnorm_bwd(Xd["r_dy"], Xd["r_x"], Xd["r_scale"], Xd["r_rms"])
+            res = {"y": y, "h_last": hl, "cdx": cdx, "cdw": cdw, "cdb": cdb, "rdx": rdx, "rds": rds}
+            res.update({k: v for k, v in g.items() if v is not None})
+            for k, v in res.items():
+                if k not in outs_host:
+                    outs_host[k] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                outs_host[k].copy_(v, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        d2h = sum(v.numel() * v.element_size() for v in outs_host.values())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1), ws, dev) / args.steps
+        e2e = {"value": elems * ws / (ms_e2e * 1e-3), "unit": UNIT, "ms_per_step": round(ms_e2e, 4),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "B": B, "L": L, "D": D, "N": N, "d_conv": K, "d_model": H, "chunk": chunk,
+                       "activations": wl.dtype, "state_and_grads": "f32", "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2 (no flush): x, delta, z, dy alone are "
+                             f"{4 * elems * (2 if wl.dtype == 'bf16' else 4) / 1e6:.0f} MB vs 129 MB L2"},
+            "roofline": roofline,
+            "scan_fwd_bwd": {"ms": round(scan_ms, 5), "elems_per_s": elems / (scan_ms * 1e-3),
+                             "alg_GB/s": round(scan_bytes / (scan_ms * 1e-3) / 1e9, 1),
+                             "frac": round(scan_bytes / (scan_ms * 1e-3) / 1e9 / peak, 4)},
+            "kernels": kern, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": launches_per_step * args.steps,
+        }), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -41,7 +41,7 @@ extern "C" {
 #define SS_OK 0
 #define SS_ERR_NULL (-1)        /* a required pointer is NULL */
 #define SS_ERR_DIM (-2)         /* a size is <= 0, or out of the supported range */
-#define SS_ERR_UNSUPPORTED (-3) /* N not in {4,8,16}, unknown dtype, d_conv not in 1..4, chunk not a multiple of 16 */
+#define SS_ERR_UNSUPPORTED (-3) /* N not in {4,8,16}, unknown dtype, d_conv not in 1..4, chunk not 8 or a multiple of 16 */
 #define SS_ERR_ALIGN (-4)       /* a pointer is not 16-byte aligned, or D / dim not a multiple of 8 */
 #define SS_ERR_WORKSPACE (-5)   /* workspace NULL or smaller than the *_workspace_size() query */
 #define SS_ERR_CUDA (-6)        /* a CUDA runtime call or kernel launch failed */
@@ -75,11 +75,13 @@ int ss_scan_num_chunks(int L, int chunk);
  *   Dv          : [D]        fp32 skip weight
  *   h0          : [B, D, N]  fp32 initial state, or NULL for zeros
  *   y           : [B, L, D]  output (dtype; bf16 is rounded to nearest even)
- *   ckpt        : [B, D, ceil(L/chunk), N] fp32 output: ckpt[b,d,c,:] is the
+ *   ckpt        : [B, ceil(L/chunk), D, N] fp32 output: ckpt[b,c,d,:] is the
  *                 state entering step c*chunk (c = 0 holds h0 or zeros).  The
  *                 backward rebuilds every other state from these.
  *   h_last      : [B, D, N]  fp32 final state h_{L-1}, or NULL
- *   chunk       : checkpoint interval, a positive multiple of 16
+ *   chunk       : checkpoint interval: 8, or a multiple of 16.  chunk = 8
+ *                 lets the backward skip its recompute pass at the price of
+ *                 N*4 bytes of checkpoint per 8 steps and channel.
  *   N           : 4, 8 or 16;  D: a multiple of 8
  * Alignment: every pointer 16-byte aligned.
  */
@@ -98,7 +100,7 @@ size_t ss_scan_bwd_workspace_size(int B, int L, int D, int N, int chunk, int dty
  * through ss_scan_fwd (backpropagation through time through the SSM state).
  *
  * Inputs are those of the forward plus
- *   ckpt     : [B, D, ceil(L/chunk), N] the forward's checkpoints, same chunk
+ *   ckpt     : [B, ceil(L/chunk), D, N] the forward's checkpoints, same chunk (at most 512)
  *   dy       : [B, L, D] activations (dtype): dL/dy
  *   dh_last  : [B, D, N] fp32 gradient arriving on the final state, or NULL (zero)
  * Outputs (fp32):

@@ -166,11 +166,79 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------- tensor memory
+// TMEM serves as per-thread scratch: thread i of warp w owns TMEM lane
+// 32 * (w % 4) + i and addresses its columns with the 32x32b access shape.
+
+// Allocate `ncols` columns (a power of two >= 32); the whole warp executes it
+// and the base address lands in *dst (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Store 8 floats into 8 consecutive columns of the thread's lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, float4 a, float4 b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(__float_as_uint(a.x)), "r"(__float_as_uint(a.y)), "r"(__float_as_uint(a.z)), "r"(__float_as_uint(a.w)),
+               "r"(__float_as_uint(b.x)), "r"(__float_as_uint(b.y)), "r"(__float_as_uint(b.z)), "r"(__float_as_uint(b.w))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Load 8 floats from 8 consecutive columns of the thread's lane and wait for
+// them (load and wait in one statement so no use can move above the wait).
+__device__ __forceinline__ void tmem_ld8_wait(uint32_t taddr, float4& a, float4& b) {
+  uint32_t r0, r1, r2, r3, r4, r5, r6, r7;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3), "=r"(r4), "=r"(r5), "=r"(r6), "=r"(r7)
+      : "r"(taddr)
+      : "memory");
+  a = make_float4(__uint_as_float(r0), __uint_as_float(r1), __uint_as_float(r2), __uint_as_float(r3));
+  b = make_float4(__uint_as_float(r4), __uint_as_float(r5), __uint_as_float(r6), __uint_as_float(r7));
+}
+
 // Time a kernel waits on its own TMA copies before declaring failure.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 // Device error word codes (or-ed together).
 constexpr unsigned kErrTmaTimeout = 1u;
+
+// Column sums of a [rows, ncols] fp32 partial array in a fixed order:
+// out(i) = sum_{g < rows} part[g * ncols + i], delivered to Store::put(i, v).
+// Block (32, 8): thread (x, y) adds rows g = y, y+8, ... in ascending order,
+// then the eight partial sums are added y = 0..7; deterministic run to run.
+template <class Store>
+__global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ part, long long ncols, int rows, Store st) {
+  __shared__ float red[8][33];
+  const long long i = (long long)blockIdx.x * 32 + threadIdx.x;
+  float acc = 0.f;
+  if (i < ncols)
+    for (int g = threadIdx.y; g < rows; g += 8) acc += part[(size_t)g * ncols + i];
+  red[threadIdx.y][threadIdx.x] = acc;
+  __syncthreads();
+  if (threadIdx.y == 0 && i < ncols) {
+    float v = red[0][threadIdx.x];
+#pragma unroll
+    for (int y = 1; y < 8; ++y) v += red[y][threadIdx.x];
+    st.put(i, v);
+  }
+}
+
+template <class Store>
+inline cudaError_t colsum(const float* part, long long ncols, int rows, Store st, cudaStream_t s) {
+  const long long blocks = (ncols + 31) / 32;
+  colsum_kernel<Store><<<(unsigned)blocks, dim3(32, 8), 0, s>>>(part, ncols, rows, st);
+  return cudaGetLastError();
+}
 
 }  // namespace ssk
 

@@ -8,7 +8,7 @@
 // step) over a 64-step tile of one batch row and slides two K-wide register
 // windows along time: dout ahead of the output step (for dx) and x behind it
 // (for dw).  Each CTA loops over several (batch, tile) pairs, keeping dw / db
-// in registers, and writes one partial per CTA row; conv_reduce_kernel adds
+// in registers, and writes one partial per CTA row; colsum_kernel adds
 // the partials in fixed order into dw / db.  HBM traffic is one read of dout
 // and x plus one write of dx (the K-1 halo steps per tile come from L2).
 #include "common.cuh"
@@ -86,27 +86,24 @@ __global__ void __launch_bounds__(kCThreads) conv_bwd_kernel(const float* __rest
         db = f4add(db, gw[0]);
       }
     }
-    float* o = ws + ((size_t)blockIdx.y * D + d) * (K + 1);
+    float* o = ws + (size_t)blockIdx.y * (K + 1) * D + d;  // partial row: [K+1][D]
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-      for (int k = 0; k < K; ++k) o[c * (K + 1) + k] = c == 0 ? dw[k].x : c == 1 ? dw[k].y : c == 2 ? dw[k].z : dw[k].w;
-      o[c * (K + 1) + K] = c == 0 ? db.x : c == 1 ? db.y : c == 2 ? db.z : db.w;
-    }
+    for (int k = 0; k < K; ++k) *reinterpret_cast<float4*>(o + (size_t)k * D) = dw[k];
+    *reinterpret_cast<float4*>(o + (size_t)K * D) = db;
   }
 }
 
-// dw[d,k] += sum_g ws[g][d][k];  db[d] += sum_g ws[g][d][K]
-__global__ void conv_reduce_kernel(const float* __restrict__ ws, float* dw, float* db, int D, int K, int gy) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  const int per = K + 1;
-  if (i >= D * per) return;
-  float acc = 0.f;
-  for (int g = 0; g < gy; ++g) acc += ws[(size_t)g * D * per + i];
-  const int d = i / per, k = i % per;
-  if (k < K) dw[(size_t)d * K + k] += acc;
-  else db[d] += acc;
-}
+// column i = k * D + d of the partials: dw[d, k] (k < K) or db[d] (k = K)
+struct ConvStore {
+  float* dw;
+  float* db;
+  int D, K;
+  __device__ void put(long long i, float v) const {
+    const int k = (int)(i / D), d = (int)(i % D);
+    if (k < K) dw[(size_t)d * K + k] += v;
+    else db[d] += v;
+  }
+};
 
 struct ConvPlan {
   int gx, gy;
@@ -138,9 +135,7 @@ int conv_launch(const float* dout, const void* x, const float* w, float* dx, flo
                 float* ws, const ConvPlan& pl, cudaStream_t s) {
   conv_bwd_kernel<K, T><<<dim3(pl.gx, pl.gy), kCThreads, 0, s>>>(dout, static_cast<const T*>(x), w, dx, ws, B, L, D);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
-  const int n = D * (K + 1);
-  conv_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(ws, dw, db, D, K, pl.gy);
-  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  return colsum(ws, (long long)D * (K + 1), pl.gy, ConvStore{dw, db, D, K}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 }  // namespace

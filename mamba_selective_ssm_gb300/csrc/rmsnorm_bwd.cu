@@ -9,7 +9,7 @@
 // prefetches the next row while the current row's dot product is reduced
 // (warp shuffles, then one shared-memory exchange whose buffer alternates
 // with the row parity, so one barrier per row suffices).  Per-CTA dscale
-// partials are added in fixed order by rms_reduce_kernel.
+// partials are added in fixed order by colsum_kernel.
 #include "common.cuh"
 
 namespace {
@@ -100,13 +100,10 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_kernel(const T* __rest
   }
 }
 
-__global__ void rms_reduce_kernel(const float* __restrict__ ws, float* dscale, int dim, int g) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= dim) return;
-  float a = 0.f;
-  for (int k = 0; k < g; ++k) a += ws[(size_t)k * dim + i];
-  dscale[i] += a;
-}
+struct AddTo {
+  float* out;
+  __device__ void put(long long i, float v) const { out[i] += v; }
+};
 
 struct RmsPlan {
   int vpt, threads, grid;
@@ -118,7 +115,7 @@ inline RmsPlan rms_plan(int rows, int dim) {
   const int groups = dim / 8;
   p.vpt = groups <= 1024 ? 1 : groups <= 2048 ? 2 : 4;
   p.threads = ((groups + p.vpt - 1) / p.vpt + 31) / 32 * 32;
-  p.grid = rows < 1024 ? rows : 1024;
+  p.grid = rows < 608 ? rows : 608;  // 4 waves of 152 SMs; each CTA walks rows/608 rows
   p.bytes = (size_t)p.grid * dim * sizeof(float);
   return p;
 }
@@ -140,8 +137,7 @@ int rms_launch(const void* dy, const void* x, const float* scale, const float* r
   else if (pl.vpt == 2) rms_bwd_kernel<T, 2><<<pl.grid, pl.threads, 0, s>>>(g, xx, scale, rms, dx, ws, rows, dim);
   else rms_bwd_kernel<T, 4><<<pl.grid, pl.threads, 0, s>>>(g, xx, scale, rms, dx, ws, rows, dim);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
-  rms_reduce_kernel<<<(dim + 255) / 256, 256, 0, s>>>(ws, dscale, dim, pl.grid);
-  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  return colsum(ws, dim, pl.grid, AddTo{dscale}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 }  // namespace

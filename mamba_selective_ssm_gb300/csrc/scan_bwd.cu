@@ -6,17 +6,20 @@
 // last to first; each chunk (a multiple of 16 steps) is walked twice:
 //   pass A (tiles in order):   from the chunk's checkpoint, advance
 //       h_t = a_t h_{t-1} + delta_t B_t x_t and park the state entering every
-//       8-step window in shared memory;
+//       8-step window in tensor memory (TMEM: each thread owns one TMEM lane);
 //   pass B (tiles in reverse): per 8-step window, rebuild a_t and h_t from the
 //       parked state into registers (one ex2 per cell), then run the adjoint
 //       G_t = ds_t C_t + a_{t+1} G_{t+1} backwards through the window:
 //         q_t = (a_t G_t) h_{t-1};  sum_n q_t A  and  sum_n G_t B_t  (-> ddelta, dx)
 //         dA += q_t delta_t;  dB_t += G_t delta_t x_t;  dC_t += ds_t h_t.
 //       The carry a_t G_t crosses windows, tiles and chunks in registers.
-// Sums over n are warp reduce-scatters; dB_t and dC_t (sums over d) are
-// reduced across lanes and warps, written as one partial per 64-channel tile
-// to the workspace, and summed in fixed order by ss_bwd_reduce_kernel, as are
-// the per-CTA partials of dA and dD.  No atomics: results are bitwise
+// With chunk = 8 every window has its own checkpoint and pass A is skipped.
+// Inside the step loops every thread only adds its own cells and stores its
+// shares to shared memory; the window epilogue adds the shares in a fixed
+// order (over the 4-state lane groups for the per-(t,d) sums, over lanes and
+// warps for dB_t, dC_t) and writes dx, ddelta, dz and one dB/dC partial per
+// 64-channel tile.  ss_bwd_dbc_kernel and colsum_kernel add the partials of
+// dB/dC and of dA/dD in fixed order.  No atomics: results are bitwise
 // reproducible.
 #include "scan_common.cuh"
 
@@ -26,8 +29,12 @@ using namespace ssk;
 
 __device__ unsigned g_bwd_err;
 
+constexpr int kSP = kDT + 8;        // row pitch of the C.h shares (bank spread across lane groups)
+constexpr int kSAB = 2 * kDT + 8;   // row pitch of the (sum qA, sum GB) shares
+
 template <typename T, int N, int NSTG>
 struct BwdSmem {
+  static constexpr int W = Geo<N>::W, CG = Geo<N>::CG;
   alignas(128) T dlt[NSTG][kTT * kDT];
   alignas(128) T x[NSTG][kTT * kDT];
   alignas(128) T z[NSTG][kTT * kDT];
@@ -39,19 +46,24 @@ struct BwdSmem {
   alignas(16) float ds_f[kTT * kDT];  // dy * silu(z)
   alignas(16) float B_f[kTT * N];
   alignas(16) float C_f[kTT * N];
-  alignas(16) float s_f[kTT * kDT];   // C_t . h_t
-  alignas(16) float sA_f[kTT * kDT];  // sum_n q_t A log2(e)
-  alignas(16) float sB_f[kTT * kDT];  // sum_n G_t B_t
-  alignas(16) float dBC_w[Geo<N>::W][kTT][2 * N];
+  // one 8-step window's per-lane shares
+  alignas(16) float sp[kS][N / 4][kSP];    // C_t . h_t over the lane's 4 states
+  alignas(16) float sab[kS][N / 4][kSAB];  // (sum q A log2 e, sum G B) over the lane's 4 states, per channel
+  // [warp][step][dB | dC][channel-pair group x state]: G_t delta_t x_t and ds_t h_t summed over
+  // the lane's 2 channels (row pitch CG*N + 16 keeps the epilogue's 128-bit reads conflict-free)
+  alignas(16) float dbc[W][kS][2][CG * N + 16];
   alignas(16) float Dv_s[kDT];
-  alignas(16) float dD_red[Geo<N>::NT][8];
   alignas(8) uint64_t full[NSTG];
+  uint32_t tmem_base;
 };
 
-template <typename T, int N, int NSTG>
-constexpr size_t bwd_smem_bytes(int chunk) {
-  return ((sizeof(BwdSmem<T, N, NSTG>) + 15) / 16) * 16 + (size_t)(chunk / kS) * 2 * Geo<N>::NT * sizeof(float4);
+// TMEM columns: 8 per window boundary of a chunk, rounded up to a power of two >= 32
+inline uint32_t tmem_cols(int chunk) {
+  uint32_t need = (uint32_t)(chunk / kS) * 8u, c = 32;
+  while (c < need) c <<= 1;
+  return c;
 }
+constexpr int kMaxChunk = 512;  // 64 windows x 8 columns = the 512 TMEM columns of an SM
 
 struct BwdParams {
   const float* A;
@@ -63,9 +75,9 @@ struct BwdParams {
   float* dz;
   float* dh0;
   float* ws_dBC;  // [ndt][B][L][2N]
-  float* ws_dA;   // [gy][D][N]
-  float* ws_dD;   // [gy][D]
+  float* ws_dAD;  // [gy][D*N + D]: dA then dD partials of each CTA row
   int B, L, D, chunk, nchunks;
+  uint32_t tcols;
 };
 
 template <int N, typename T, int NSTG>
@@ -79,7 +91,6 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
   using AT = ActT<T>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BwdSmem<T, N, NSTG>& S = *reinterpret_cast<BwdSmem<T, N, NSTG>*>(smem_raw);
-  float4* bnd = reinterpret_cast<float4*>(smem_raw + ((sizeof(BwdSmem<T, N, NSTG>) + 15) / 16) * 16);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ng = lane % G::NG, cg = lane / G::NG;
@@ -92,7 +103,8 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
   const int ntiles = (L + kTT - 1) / kTT;
   const int tpc = p.chunk / kTT;                        // tiles per full chunk
   const int ntl = ntiles - (p.nchunks - 1) * tpc;       // tiles in the last chunk
-  const int per_b = 2 * ntiles;                         // items per batch row
+  const bool direct = p.chunk == kS;                    // a checkpoint per window: no pass A
+  const int per_b = direct ? ntiles : 2 * ntiles;       // items per batch row
   const int nb = (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
   const int nitems = nb * per_b;
   constexpr uint32_t kActBytes = kTT * kDT * AT::kBytes;
@@ -112,28 +124,39 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
     }
   for (int c = tid; c < kDT; c += G::NT) S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
 
-  // item k -> (batch row, chunk, tile within chunk, pass)
-  auto decode = [&](int k, int& b, int& kc, int& tl, bool& passB) {
+  // item k -> (batch row, tile of the sequence, pass; lastA: last pass-A tile of its chunk)
+  auto decode = [&](int k, int& b, int& gt, bool& passB, bool& lastA) {
     b = (int)blockIdx.y + (k / per_b) * (int)gridDim.y;
     const int q = k % per_b;
+    if (direct) {
+      gt = ntiles - 1 - q;
+      passB = true;
+      lastA = false;
+      return;
+    }
+    int kc, tl, ntc;
     if (q < 2 * ntl) {
       kc = p.nchunks - 1;
+      ntc = ntl;
       passB = q >= ntl;
       tl = passB ? ntl - 1 - (q - ntl) : q;
     } else {
       const int q2 = q - 2 * ntl;
       kc = p.nchunks - 2 - q2 / (2 * tpc);
+      ntc = tpc;
       const int r = q2 % (2 * tpc);
       passB = r >= tpc;
       tl = passB ? tpc - 1 - (r - tpc) : r;
     }
+    gt = kc * tpc + tl;
+    lastA = !passB && tl == ntc - 1;
   };
   auto issue = [&](int k) {
-    int b, kc, tl;
-    bool passB;
-    decode(k, b, kc, tl, passB);
+    int b, gt;
+    bool passB, lastA;
+    decode(k, b, gt, passB, lastA);
     const int slot = k % NSTG;
-    const int t0 = (kc * tpc + tl) * kTT;
+    const int t0 = gt * kTT;
     mbar_arrive_expect_tx(&S.full[slot], passB ? 4 * kActBytes + 2 * kBCBytes : 2 * kActBytes + kBCBytes);
     tma_load_3d(S.dlt[slot], &tm_dlt, &S.full[slot], d0, t0, b);
     tma_load_3d(S.x[slot], &tm_x, &S.full[slot], d0, t0, b);
@@ -145,6 +168,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
     }
   };
 
+  if (warp == 0 && !direct) tmem_alloc(&S.tmem_base, p.tcols);
   if (tid == 0) {
     prefetch_tmap(&tm_dlt); prefetch_tmap(&tm_x); prefetch_tmap(&tm_z);
     prefetch_tmap(&tm_dy); prefetch_tmap(&tm_B); prefetch_tmap(&tm_C);
@@ -152,23 +176,29 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
     fence_barrier_init();
     for (int k = 0; k < NSTG && k < nitems; ++k) issue(k);
   }
+  tc_fence_before_sync();
   __syncthreads();
+  tc_fence_after_sync();
+  // this thread's TMEM lane: 32 * (warp % 4) + lane; window boundary sb at columns [8 sb, 8 sb + 8)
+  const uint32_t tlane = direct ? 0u : S.tmem_base + ((uint32_t)(32 * (warp & 3)) << 16);
 
   float2 h[2][2];              // pass-A running state
   float2 ga[2][2];             // a_{t+1} * G_{t+1}: the adjoint carried backwards
   float2 dA2[2][2];            // dA partial sums of the thread's cells
-  float dDacc[8];              // dD partial sums of the epilogue channel group
+  float dDacc[4];              // dD partial sums of the epilogue's four channels
 #pragma unroll
   for (int j = 0; j < 2; ++j) dA2[j][0] = dA2[j][1] = f2(0.f, 0.f);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) dDacc[e] = 0.f;
+  for (int e = 0; e < 4; ++e) dDacc[e] = 0.f;
+  bool failed = false;
 
   for (int k = 0; k < nitems; ++k) {
     const int slot = k % NSTG;
-    int b, kc, tl;
-    bool passB;
-    decode(k, b, kc, tl, passB);
-    const int t0 = (kc * tpc + tl) * kTT;
+    int b, gt;
+    bool passB, lastA;
+    decode(k, b, gt, passB, lastA);
+    const int t0 = gt * kTT;
+    const int kc = gt / tpc, tl = gt % tpc;
 
     if (k % per_b == 0) {  // entering batch row b: the gradient arriving on h_{L-1}
 #pragma unroll
@@ -189,7 +219,8 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
         for (int k2 = k; k2 < k + NSTG && k2 < nitems; ++k2)
           mbar_wait_bounded(&S.full[k2 % NSTG], (k2 / NSTG) & 1, 100000000ull);
       }
-      return;
+      failed = true;
+      break;
     }
 
     if (!passB) {
@@ -198,23 +229,17 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (dvalid) v = *reinterpret_cast<const float4*>(p.ckpt + (((size_t)b * p.D + dg + j) * p.nchunks + kc) * N + n0);
+          if (dvalid) v = *reinterpret_cast<const float4*>(p.ckpt + (((size_t)b * p.nchunks + kc) * p.D + dg + j) * N + n0);
           h[j][0] = f2(v.x, v.y);
           h[j][1] = f2(v.z, v.w);
         }
       }
-      for (int gi = tid; gi < kTT * kDT / 8; gi += G::NT) {
-        float dv[8], xv[8];
-        AT::ld8(&S.dlt[slot][gi * 8], dv);
-        AT::ld8(&S.x[slot][gi * 8], xv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) xv[e] *= dv[e];
-        float4* a = reinterpret_cast<float4*>(&S.dlt_f[gi * 8]);
-        a[0] = make_float4(dv[0], dv[1], dv[2], dv[3]);
-        a[1] = make_float4(dv[4], dv[5], dv[6], dv[7]);
-        float4* c = reinterpret_cast<float4*>(&S.dx_f[gi * 8]);
-        c[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
-        c[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+      for (int gi = tid; gi < kTT * kDT / 4; gi += G::NT) {
+        float dv[4], xv[4];
+        AT::ld4(&S.dlt[slot][gi * 4], dv);
+        AT::ld4(&S.x[slot][gi * 4], xv);
+        reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
+        reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(dv[0] * xv[0], dv[1] * xv[1], dv[2] * xv[2], dv[3] * xv[3]);
       }
       for (int gi = tid; gi < kTT * N / 4; gi += G::NT) {
         float bv[4];
@@ -223,50 +248,68 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
       }
       __syncthreads();
 #pragma unroll
-      for (int r = 0; r < kTT; ++r) {
-        if (r % kS == 0) {
-          const int sb = (tl * kTT + r) / kS;
-          bnd[(sb * 2 + 0) * G::NT + tid] = make_float4(h[0][0].x, h[0][0].y, h[0][1].x, h[0][1].y);
-          bnd[(sb * 2 + 1) * G::NT + tid] = make_float4(h[1][0].x, h[1][0].y, h[1][1].x, h[1][1].y);
-        }
-        const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[r * kDT + dl]);
-        const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * kDT + dl]);
-        const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
-        const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
+      for (int half = 0; half < kTT / kS; ++half) {
+        tmem_st8(tlane + (uint32_t)((tl * (kTT / kS) + half) * 8),
+                 make_float4(h[0][0].x, h[0][0].y, h[0][1].x, h[0][1].y),
+                 make_float4(h[1][0].x, h[1][0].y, h[1][1].x, h[1][1].y));
+        float2 av[kS][2][2];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float2 dj = bc2(j ? dd.y : dd.x);
-          const float2 xj = bc2(j ? xx.y : xx.x);
-          h[j][0] = fma2(ex2_2(mul2(dj, Ap[j][0])), h[j][0], mul2(xj, B01));
-          h[j][1] = fma2(ex2_2(mul2(dj, Ap[j][1])), h[j][1], mul2(xj, B23));
+        for (int i = 0; i < kS; ++i) {  // exponentials first: independent of the state
+          const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[(half * kS + i) * kDT + dl]);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float2 dj = bc2(j ? dd.y : dd.x);
+            av[i][j][0] = ex2_2(mul2(dj, Ap[j][0]));
+            av[i][j][1] = ex2_2(mul2(dj, Ap[j][1]));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kS; ++i) {
+          const int r = half * kS + i;
+          const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * kDT + dl]);
+          const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
+          const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float2 xj = bc2(j ? xx.y : xx.x);
+            h[j][0] = fma2(av[i][j][0], h[j][0], mul2(xj, B01));
+            h[j][1] = fma2(av[i][j][1], h[j][1], mul2(xj, B23));
+          }
         }
       }
+      if (lastA) tmem_wait_st();  // the chunk's states are parked before pass B reads them
       __syncthreads();
       if (tid == 0 && k + NSTG < nitems) issue(k + NSTG);
       continue;
     }
 
     // -------------------------------------------------- pass B: adjoint sweep
-    for (int gi = tid; gi < kTT * kDT / 8; gi += G::NT) {
-      float dv[8], xv[8], zv[8], gv[8];
-      AT::ld8(&S.dlt[slot][gi * 8], dv);
-      AT::ld8(&S.x[slot][gi * 8], xv);
-      AT::ld8(&S.z[slot][gi * 8], zv);
-      AT::ld8(&S.dy[slot][gi * 8], gv);
+    float4 hck[kTT / kS][2];  // direct mode: the checkpoints entering the tile's two windows
+    if (direct) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
+      for (int w = 0; w < kTT / kS; ++w)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = gt * (kTT / kS) + w;
+          hck[w][j] = (dvalid && c < p.nchunks)
+                          ? *reinterpret_cast<const float4*>(p.ckpt + (((size_t)b * p.nchunks + c) * p.D + dg + j) * N + n0)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    for (int gi = tid; gi < kTT * kDT / 4; gi += G::NT) {
+      float dv[4], xv[4], zv[4], gv[4];
+      AT::ld4(&S.dlt[slot][gi * 4], dv);
+      AT::ld4(&S.x[slot][gi * 4], xv);
+      AT::ld4(&S.z[slot][gi * 4], zv);
+      AT::ld4(&S.dy[slot][gi * 4], gv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
         xv[e] *= dv[e];
         gv[e] *= zv[e] * sigmoid(zv[e]);
       }
-      float4* a = reinterpret_cast<float4*>(&S.dlt_f[gi * 8]);
-      a[0] = make_float4(dv[0], dv[1], dv[2], dv[3]);
-      a[1] = make_float4(dv[4], dv[5], dv[6], dv[7]);
-      float4* c = reinterpret_cast<float4*>(&S.dx_f[gi * 8]);
-      c[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
-      c[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
-      float4* s = reinterpret_cast<float4*>(&S.ds_f[gi * 8]);
-      s[0] = make_float4(gv[0], gv[1], gv[2], gv[3]);
-      s[1] = make_float4(gv[4], gv[5], gv[6], gv[7]);
+      reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
+      reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(xv[0], xv[1], xv[2], xv[3]);
+      reinterpret_cast<float4*>(S.ds_f)[gi] = make_float4(gv[0], gv[1], gv[2], gv[3]);
     }
     for (int gi = tid; gi < kTT * N / 4; gi += G::NT) {
       float bv[4], cv[4];
@@ -277,22 +320,35 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
     }
     __syncthreads();
 
-    const int dsi = dsum_index(lane);
-    const bool dsw = (lane & G::kDupMask) == 0;
     for (int sub = kTT / kS - 1; sub >= 0; --sub) {
       const int sb = tl * (kTT / kS) + sub;
       float2 hb[2][2];
       {
-        const float4 v0 = bnd[(sb * 2 + 0) * G::NT + tid], v1 = bnd[(sb * 2 + 1) * G::NT + tid];
+        float4 v0, v1;
+        if (direct) {
+          v0 = sub ? hck[1][0] : hck[0][0];
+          v1 = sub ? hck[1][1] : hck[0][1];
+        } else {
+          tmem_ld8_wait(tlane + (uint32_t)(sb * 8), v0, v1);
+        }
         hb[0][0] = f2(v0.x, v0.y); hb[0][1] = f2(v0.z, v0.w);
         hb[1][0] = f2(v1.x, v1.y); hb[1][1] = f2(v1.z, v1.w);
       }
       float2 av[kS][2][2], hv[kS][2][2];
-      // rebuild the window: a_t and h_t in registers, C.h and dC on the way
+#pragma unroll
+      for (int i = 0; i < kS; ++i) {  // exponentials first: independent of the state
+        const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[(sub * kS + i) * kDT + dl]);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float2 dj = bc2(j ? dd.y : dd.x);
+          av[i][j][0] = ex2_2(mul2(dj, Ap[j][0]));
+          av[i][j][1] = ex2_2(mul2(dj, Ap[j][1]));
+        }
+      }
+      // rebuild the window's states; shares of C.h and dC on the way
 #pragma unroll
       for (int i = 0; i < kS; ++i) {
         const int r = sub * kS + i;
-        const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[r * kDT + dl]);
         const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * kDT + dl]);
         const float2 gg = *reinterpret_cast<const float2*>(&S.ds_f[r * kDT + dl]);
         const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
@@ -303,13 +359,10 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
         float2 dc0, dc1;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const float2 dj = bc2(j ? dd.y : dd.x);
           const float2 xj = bc2(j ? xx.y : xx.x);
           const float2 gj = bc2(j ? gg.y : gg.x);
           const float2 hp0 = i ? hv[i - 1][j][0] : hb[j][0];
           const float2 hp1 = i ? hv[i - 1][j][1] : hb[j][1];
-          av[i][j][0] = ex2_2(mul2(dj, Ap[j][0]));
-          av[i][j][1] = ex2_2(mul2(dj, Ap[j][1]));
           hv[i][j][0] = fma2(av[i][j][0], hp0, mul2(xj, B01));
           hv[i][j][1] = fma2(av[i][j][1], hp1, mul2(xj, B23));
           const float2 yy = fma2(C23, hv[i][j][1], mul2(C01, hv[i][j][0]));
@@ -322,22 +375,8 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
             dc1 = fma2(gj, hv[i][1][1], dc1);
           }
         }
-        if constexpr (G::NG == 4) {
-          const bool up = ng & 2;
-          float keep = up ? yj[1] : yj[0];
-          keep += __shfl_xor_sync(0xffffffffu, up ? yj[0] : yj[1], 2);
-          keep += __shfl_xor_sync(0xffffffffu, keep, 1);
-          if ((ng & 1) == 0) S.s_f[r * kDT + dl + (ng >> 1)] = keep;
-        } else if constexpr (G::NG == 2) {
-          const bool up = ng & 1;
-          float keep = up ? yj[1] : yj[0];
-          keep += __shfl_xor_sync(0xffffffffu, up ? yj[0] : yj[1], 1);
-          S.s_f[r * kDT + dl + ng] = keep;
-        } else {
-          *reinterpret_cast<float2*>(&S.s_f[r * kDT + dl]) = f2(yj[0], yj[1]);
-        }
-        const float dcs = dsum4<N>(dc0.x, dc0.y, dc1.x, dc1.y, lane);
-        if (dsw) S.dBC_w[warp][r][N + n0 + dsi] = dcs;
+        *reinterpret_cast<float2*>(&S.sp[i][ng][dl]) = f2(yj[0], yj[1]);
+        *reinterpret_cast<float4*>(&S.dbc[warp][i][1][cg * N + n0]) = make_float4(dc0.x, dc0.y, dc1.x, dc1.y);
       }
       // adjoint sweep backwards through the window
 #pragma unroll
@@ -379,76 +418,76 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
             db1 = fma2(G1, xj, db1);
           }
         }
-        // sums over n of the pair group: (sA0, sA1, sB0, sB1)
-        if constexpr (G::NG == 4) {
-          const bool up = ng & 2;
-          float k0 = up ? sB[0] : sA[0], k1 = up ? sB[1] : sA[1];
-          k0 += __shfl_xor_sync(0xffffffffu, up ? sA[0] : sB[0], 2);
-          k1 += __shfl_xor_sync(0xffffffffu, up ? sA[1] : sB[1], 2);
-          const bool up1 = ng & 1;
-          float kk = up1 ? k1 : k0;
-          kk += __shfl_xor_sync(0xffffffffu, up1 ? k0 : k1, 1);
-          (up ? S.sB_f : S.sA_f)[r * kDT + dl + (ng & 1)] = kk;
-        } else if constexpr (G::NG == 2) {
-          const bool up = ng & 1;
-          float k0 = up ? sB[0] : sA[0], k1 = up ? sB[1] : sA[1];
-          k0 += __shfl_xor_sync(0xffffffffu, up ? sA[0] : sB[0], 1);
-          k1 += __shfl_xor_sync(0xffffffffu, up ? sA[1] : sB[1], 1);
-          *reinterpret_cast<float2*>(&(up ? S.sB_f : S.sA_f)[r * kDT + dl]) = f2(k0, k1);
-        } else {
-          *reinterpret_cast<float2*>(&S.sA_f[r * kDT + dl]) = f2(sA[0], sA[1]);
-          *reinterpret_cast<float2*>(&S.sB_f[r * kDT + dl]) = f2(sB[0], sB[1]);
-        }
-        const float dbs = dsum4<N>(db0.x, db0.y, db1.x, db1.y, lane);
-        if (dsw) S.dBC_w[warp][r][n0 + dsi] = dbs;
+        *reinterpret_cast<float4*>(&S.sab[i][ng][2 * dl]) = make_float4(sA[0], sB[0], sA[1], sB[1]);
+        *reinterpret_cast<float4*>(&S.dbc[warp][i][0][cg * N + n0]) = make_float4(db0.x, db0.y, db1.x, db1.y);
       }
-    }
-    __syncthreads();
+      __syncthreads();
 
-    // dB_t, dC_t of this 64-channel tile: sum over warps in fixed order
-    for (int e = tid; e < kTT * 2 * N; e += G::NT) {
-      const int r = e / (2 * N), c = e % (2 * N);
-      const int t = t0 + r;
-      if (t < L) {
-        float acc = S.dBC_w[0][r][c];
+      // window epilogue.  dB_t, dC_t of this tile of 64 channels: lanes and warps in fixed order
+      for (int e = tid; e < kS * N / 2; e += G::NT) {  // (row, dB | dC, group of 4 states)
+        const int i = e / (N / 2), qq = (e % (N / 2)) / (N / 4), n4 = (e % (N / 4)) * 4;
+        const int t = t0 + sub * kS + i;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 1; w < G::W; ++w) acc += S.dBC_w[w][r][c];
-        p.ws_dBC[(((size_t)blockIdx.x * p.B + b) * L + t) * (2 * N) + c] = acc;
+        for (int w = 0; w < G::W; ++w)
+#pragma unroll
+          for (int c = 0; c < G::CG; ++c) {
+            const float4 v = *reinterpret_cast<const float4*>(&S.dbc[w][i][qq][c * N + n4]);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+          }
+        if (t < L)
+          *reinterpret_cast<float4*>(&p.ws_dBC[(((size_t)blockIdx.x * p.B + b) * L + t) * (2 * N) + qq * N + n4]) = acc;
       }
-    }
-    // per-(t, d) gradients
-    for (int gi = tid; gi < kTT * kDT / 8; gi += G::NT) {
-      const int r = gi / (kDT / 8), c8 = (gi % (kDT / 8)) * 8;
-      const int t = t0 + r, d = d0 + c8;
-      if (t < L && d < p.D) {
-        float dv[8], xv[8], zv[8], gv[8], o0[8], o1[8], o2[8];
-        AT::ld8(&S.dlt[slot][r * kDT + c8], dv);
-        AT::ld8(&S.x[slot][r * kDT + c8], xv);
-        AT::ld8(&S.z[slot][r * kDT + c8], zv);
-        AT::ld8(&S.dy[slot][r * kDT + c8], gv);
+      // per-(t, d) gradients, four channels per thread
+      for (int gi = tid; gi < kS * kDT / 4; gi += G::NT) {
+        const int i = gi / (kDT / 4), c4 = (gi % (kDT / 4)) * 4;
+        const int rr = sub * kS + i;
+        const int t = t0 + rr, d = d0 + c4;
+        if (t < L && d < p.D) {
+          float dv[4], xv[4], zv[4], gv[4], o0[4], o1[4], o2[4];
+          AT::ld4(&S.dlt[slot][rr * kDT + c4], dv);
+          AT::ld4(&S.x[slot][rr * kDT + c4], xv);
+          AT::ld4(&S.z[slot][rr * kDT + c4], zv);
+          AT::ld4(&S.dy[slot][rr * kDT + c4], gv);
+          float4 sv = *reinterpret_cast<const float4*>(&S.sp[i][0][c4]);
+          float4 ab0 = *reinterpret_cast<const float4*>(&S.sab[i][0][2 * c4]);
+          float4 ab1 = *reinterpret_cast<const float4*>(&S.sab[i][0][2 * c4 + 4]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int o = r * kDT + c8 + e;
-          const float Dd = S.Dv_s[c8 + e];
-          const float sg = sigmoid(zv[e]);
-          const float s = S.s_f[o] + Dd * xv[e];
-          const float ds = S.ds_f[o];
-          const float sB = S.sB_f[o];
-          o0[e] = ds * Dd + dv[e] * sB;                      // dx
-          o1[e] = S.sA_f[o] * kLn2 + xv[e] * sB;             // ddelta
-          o2[e] = gv[e] * s * sg * (1.0f + zv[e] * (1.0f - sg));  // dz
-          dDacc[e] += ds * xv[e];
+          for (int g = 1; g < N / 4; ++g) {
+            const float4 u = *reinterpret_cast<const float4*>(&S.sp[i][g][c4]);
+            const float4 v0 = *reinterpret_cast<const float4*>(&S.sab[i][g][2 * c4]);
+            const float4 v1 = *reinterpret_cast<const float4*>(&S.sab[i][g][2 * c4 + 4]);
+            sv.x += u.x; sv.y += u.y; sv.z += u.z; sv.w += u.w;
+            ab0.x += v0.x; ab0.y += v0.y; ab0.z += v0.z; ab0.w += v0.w;
+            ab1.x += v1.x; ab1.y += v1.y; ab1.z += v1.z; ab1.w += v1.w;
+          }
+          const float4 dsv = *reinterpret_cast<const float4*>(&S.ds_f[rr * kDT + c4]);
+          const float4 Dd4 = *reinterpret_cast<const float4*>(&S.Dv_s[c4]);
+          const float shv[4] = {sv.x, sv.y, sv.z, sv.w};
+          const float sAv[4] = {ab0.x, ab0.z, ab1.x, ab1.z};
+          const float sBv[4] = {ab0.y, ab0.w, ab1.y, ab1.w};
+          const float dsa[4] = {dsv.x, dsv.y, dsv.z, dsv.w};
+          const float Dd[4] = {Dd4.x, Dd4.y, Dd4.z, Dd4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float sg = sigmoid(zv[e]);
+            const float s = fmaf(Dd[e], xv[e], shv[e]);
+            o0[e] = fmaf(dsa[e], Dd[e], dv[e] * sBv[e]);                 // dx
+            o1[e] = fmaf(sAv[e], kLn2, xv[e] * sBv[e]);                  // ddelta
+            o2[e] = gv[e] * s * sg * fmaf(zv[e], 1.0f - sg, 1.0f);     // dz
+            dDacc[e] = fmaf(dsa[e], xv[e], dDacc[e]);
+          }
+          const size_t off = ((size_t)b * L + t) * p.D + d;
+          *reinterpret_cast<float4*>(p.dx + off) = make_float4(o0[0], o0[1], o0[2], o0[3]);
+          *reinterpret_cast<float4*>(p.ddelta + off) = make_float4(o1[0], o1[1], o1[2], o1[3]);
+          *reinterpret_cast<float4*>(p.dz + off) = make_float4(o2[0], o2[1], o2[2], o2[3]);
         }
-        const size_t off = ((size_t)b * L + t) * p.D + d;
-        ActT<float>::st8(p.dx + off, o0);
-        ActT<float>::st8(p.ddelta + off, o1);
-        ActT<float>::st8(p.dz + off, o2);
       }
+      __syncthreads();
     }
-    __syncthreads();
     if (tid == 0 && k + NSTG < nitems) issue(k + NSTG);
 
-    if (kc == 0 && tl == 0 && p.dh0 != nullptr && dvalid) {  // last item of batch row b: ga = a_0 G_0
+    if (t0 == 0 && p.dh0 != nullptr && dvalid) {  // last item of batch row b: ga = a_0 G_0
 #pragma unroll
       for (int j = 0; j < 2; ++j)
         *reinterpret_cast<float4*>(p.dh0 + ((size_t)b * p.D + dg + j) * N + n0) =
@@ -456,59 +495,62 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
     }
   }
 
+  // release the tensor memory (every warp is past its last TMEM access)
+  if (!direct) tmem_wait_st();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 0 && !direct) tmem_dealloc(S.tmem_base, p.tcols);
+  if (failed) return;
+
   // per-CTA partials of dA and dD (summed over this CTA's batch rows)
   if (dvalid) {
 #pragma unroll
     for (int j = 0; j < 2; ++j)
-      *reinterpret_cast<float4*>(p.ws_dA + ((size_t)blockIdx.y * p.D + dg + j) * N + n0) =
+      *reinterpret_cast<float4*>(p.ws_dAD + (size_t)blockIdx.y * p.D * (N + 1) + (size_t)(dg + j) * N + n0) =
           make_float4(dA2[j][0].x, dA2[j][0].y, dA2[j][1].x, dA2[j][1].y);
   }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) S.dD_red[tid][e] = dDacc[e];
+  // dD: threads with equal tid % 16 hold the same four channels
+  float* red = &S.sab[0][0][0];  // free after the last window
+  *reinterpret_cast<float4*>(&red[tid * 4]) = make_float4(dDacc[0], dDacc[1], dDacc[2], dDacc[3]);
   __syncthreads();
   for (int c = tid; c < kDT; c += G::NT) {
     if (d0 + c < p.D) {
-      const int grp = c / 8, e = c % 8;
+      const int grp = c / 4, e = c % 4;
       float acc = 0.f;
-      for (int m = grp; m < G::NT; m += kDT / 8) acc += S.dD_red[m][e];
-      p.ws_dD[(size_t)blockIdx.y * p.D + d0 + c] = acc;
+      for (int m = grp; m < G::NT; m += kDT / 4) acc += red[m * 4 + e];
+      p.ws_dAD[(size_t)blockIdx.y * p.D * (N + 1) + (size_t)p.D * N + d0 + c] = acc;
     }
   }
 }
 
-// dB, dC = sum over channel tiles (overwrite); dA, dD += sum over CTA rows.
+// dB, dC = sum over the 64-channel tiles in tile order (overwrite).
 template <int N>
-__global__ void ss_bwd_reduce_kernel(const float* __restrict__ ws_dBC, const float* __restrict__ ws_dA,
-                                     const float* __restrict__ ws_dD, float* dB, float* dC, float* dA, float* dD, int B,
-                                     int L, int D, int ndt, int gy) {
-  const long long nBC = (long long)B * L * 2 * N;
-  const long long nA = (long long)D * N;
-  const long long total = nBC + nA + D;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
-    if (i < nBC) {
-      float acc = 0.f;
-      for (int t = 0; t < ndt; ++t) acc += ws_dBC[(size_t)t * nBC + i];
-      const long long row = i / (2 * N);
-      const int c = (int)(i % (2 * N));
-      if (c < N) dB[row * N + c] = acc;
-      else dC[row * N + (c - N)] = acc;
-    } else if (i < nBC + nA) {
-      const long long j = i - nBC;
-      float acc = 0.f;
-      for (int g = 0; g < gy; ++g) acc += ws_dA[(size_t)g * nA + j];
-      dA[j] += acc;
-    } else {
-      const long long j = i - nBC - nA;
-      float acc = 0.f;
-      for (int g = 0; g < gy; ++g) acc += ws_dD[(size_t)g * D + j];
-      dD[j] += acc;
-    }
+__global__ void ss_bwd_dbc_kernel(const float* __restrict__ ws_dBC, float* dB, float* dC, long long nBC, int ndt) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nBC; i += (long long)gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int t = 0; t < ndt; ++t) acc += ws_dBC[(size_t)t * nBC + i];
+    const long long row = i / (2 * N);
+    const int c = (int)(i % (2 * N));
+    if (c < N) dB[row * N + c] = acc;
+    else dC[row * N + (c - N)] = acc;
   }
 }
+
+// dA (first D*N columns of a partial row) and dD (last D columns) accumulate.
+struct DADStore {
+  float* dA;
+  float* dD;
+  long long nA;
+  __device__ void put(long long i, float v) const {
+    if (i < nA) dA[i] += v;
+    else dD[i - nA] += v;
+  }
+};
 
 struct BwdPlan {
   int ndt, gy;
-  size_t off_dA, off_dD, total;
+  size_t off_dAD, total;
 };
 
 inline BwdPlan make_plan(int B, int L, int D, int N) {
@@ -517,10 +559,8 @@ inline BwdPlan make_plan(int B, int L, int D, int N) {
   const int cap = 1024 / pl.ndt > 0 ? 1024 / pl.ndt : 1;
   pl.gy = B < cap ? B : cap;
   const size_t bc = (size_t)pl.ndt * B * L * 2 * N * sizeof(float);
-  pl.off_dA = (bc + 255) & ~(size_t)255;
-  const size_t a = (size_t)pl.gy * D * N * sizeof(float);
-  pl.off_dD = (pl.off_dA + a + 255) & ~(size_t)255;
-  pl.total = pl.off_dD + (size_t)pl.gy * D * sizeof(float);
+  pl.off_dAD = (bc + 255) & ~(size_t)255;
+  pl.total = pl.off_dAD + (size_t)pl.gy * D * (N + 1) * sizeof(float);
   return pl;
 }
 
@@ -530,20 +570,14 @@ struct Stages {
   static constexpr int value = sizeof(T) == 4 ? 2 : 3;
 };
 
-template <int N, typename T>
-size_t bwd_smem(int chunk) {
-  return bwd_smem_bytes<T, N, Stages<T>::value>(chunk);
-}
-
-template <int N, typename T>
+template <int N, typename T, int NSTG = Stages<T>::value>
 int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, const void* dy,
                float* dA, float* dB, float* dC, float* dD, void* ws, cudaStream_t stream) {
   constexpr int e = ActT<T>::kBytes;
-  constexpr int NSTG = Stages<T>::value;
   const BwdPlan pl = make_plan(p.B, p.L, p.D, N);
   p.ws_dBC = static_cast<float*>(ws);
-  p.ws_dA = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_dA);
-  p.ws_dD = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_dD);
+  p.ws_dAD = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_dAD);
+  p.tcols = p.chunk == kS ? 0u : tmem_cols(p.chunk);
   CUtensorMap tm[6];
   const uint64_t adims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
   const uint64_t astr[2] = {(uint64_t)p.D * e, (uint64_t)p.L * p.D * e};
@@ -558,33 +592,42 @@ int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, co
       !ssh::encode_tiled(&tm[4], ActT<T>::kTma, 2, Bm, bdims, bstr, bbox) ||
       !ssh::encode_tiled(&tm[5], ActT<T>::kTma, 2, Cm, bdims, bstr, bbox))
     return SS_ERR_CUDA;
-  const size_t smem = bwd_smem<N, T>(p.chunk);
+  const size_t smem = sizeof(BwdSmem<T, N, NSTG>);
   auto kern = scan_bwd_kernel<N, T, NSTG>;
+  // TMEM: the CTAs resident on one SM must fit in its 512 columns, else an
+  // allocation would wait for another CTA to finish.  Ask for enough shared
+  // memory per CTA to keep the residency within that bound.
+  size_t smem_launch = smem;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
-  kern<<<dim3(pl.ndt, pl.gy), Geo<N>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4], tm[5]);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Geo<N>::NT, smem) != cudaSuccess) return SS_ERR_CUDA;
+  if (p.tcols != 0 && (uint32_t)per_sm * p.tcols > 512u) {
+    const int max_ctas = 512 / (int)p.tcols;
+    smem_launch = (size_t)(227 * 1024) / (size_t)(max_ctas + 1) + 1024;
+    if (smem_launch < smem) smem_launch = smem;
+    if (smem_launch > 227 * 1024) smem_launch = 227 * 1024;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_launch) != cudaSuccess)
+      return SS_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Geo<N>::NT, smem_launch) != cudaSuccess)
+      return SS_ERR_CUDA;
+    if ((uint32_t)per_sm * p.tcols > 512u) return SS_ERR_UNSUPPORTED;
+  }
+  kern<<<dim3(pl.ndt, pl.gy), Geo<N>::NT, smem_launch, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4], tm[5]);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
-  const long long total = (long long)p.B * p.L * 2 * N + (long long)p.D * N + p.D;
-  long long blocks = (total + 255) / 256;
-  if (blocks > 4096) blocks = 4096;
-  ss_bwd_reduce_kernel<N><<<(int)blocks, 256, 0, stream>>>(p.ws_dBC, p.ws_dA, p.ws_dD, dB, dC, dA, dD, p.B, p.L, p.D,
-                                                           pl.ndt, pl.gy);
-  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
-}
-
-constexpr size_t kMaxSmem = 227 * 1024;
-
-bool bwd_chunk_fits(int N, int dtype, int chunk) {
-  size_t s;
-  if (dtype == SS_F32) s = N == 4 ? bwd_smem<4, float>(chunk) : N == 8 ? bwd_smem<8, float>(chunk) : bwd_smem<16, float>(chunk);
-  else s = N == 4 ? bwd_smem<4, __nv_bfloat16>(chunk) : N == 8 ? bwd_smem<8, __nv_bfloat16>(chunk) : bwd_smem<16, __nv_bfloat16>(chunk);
-  return s <= kMaxSmem;
+  const long long nBC = (long long)p.B * p.L * 2 * N;
+  long long blocks = (nBC + 255) / 256;
+  if (blocks > 8192) blocks = 8192;
+  ss_bwd_dbc_kernel<N><<<(int)blocks, 256, 0, stream>>>(p.ws_dBC, dB, dC, nBC, pl.ndt);
+  if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+  const long long nA = (long long)p.D * N;
+  return colsum(p.ws_dAD, nA + p.D, pl.gy, DADStore{dA, dD, nA}, stream) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 int validate_bwd(int B, int L, int D, int N, int chunk, int dtype) {
   if (B <= 0 || L <= 0 || D <= 0 || N <= 0 || chunk <= 0) return SS_ERR_DIM;
   if (N != 4 && N != 8 && N != 16) return SS_ERR_UNSUPPORTED;
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
-  if (chunk % kTT != 0 || !bwd_chunk_fits(N, dtype, chunk)) return SS_ERR_UNSUPPORTED;
+  if ((chunk != kS && chunk % kTT != 0) || chunk > kMaxChunk) return SS_ERR_UNSUPPORTED;
   if (D % 8 != 0) return SS_ERR_ALIGN;
   if (((long long)L * N * (dtype == SS_F32 ? 4 : 2)) % 16 != 0) return SS_ERR_ALIGN;
   if ((long long)L * N >= (1ll << 31) || (long long)L * D >= (1ll << 40)) return SS_ERR_DIM;
@@ -622,7 +665,7 @@ extern "C" int ss_scan_bwd(const void* x, const void* delta, const float* A, con
   const BwdPlan pl = make_plan(B, L, D, N);
   if (workspace == nullptr || ws_bytes < pl.total) return SS_ERR_WORKSPACE;
   if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
-  BwdParams p{A, Dv, ckpt, dh_last, dx, ddelta, dz, dh0, nullptr, nullptr, nullptr, B, L, D, chunk, ss_scan_num_chunks(L, chunk)};
+  BwdParams p{A, Dv, ckpt, dh_last, dx, ddelta, dz, dh0, nullptr, nullptr, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 0};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SS_F32) {
     if (N == 4) return launch_bwd<4, float>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);

@@ -12,7 +12,8 @@
 //      lanes of a channel pair reduce C_t . h_t across states;
 //   4. the tile epilogue forms y = (s + D x) * silu(z) with 16-byte stores;
 //   5. thread 0 re-arms the freed stage with the tile NST ahead.
-// The state entering step c*chunk is stored as checkpoint c for the backward.
+// The state entering step c*chunk is stored as checkpoint c ([B, chunks, D, N])
+// for the backward.
 #include "scan_common.cuh"
 
 namespace {
@@ -22,6 +23,18 @@ using namespace ssk;
 __device__ unsigned g_fwd_err;
 
 constexpr int kNST = 4;  // TMA pipeline depth (tiles in flight)
+
+// Forward geometry: CPT channels x 4 states per thread (CPT = 1 doubles the
+// warps per SM relative to the backward's 2 x 4 cells, which the forward can
+// afford because it keeps no per-step history).
+template <int N, int CPT>
+struct GeoF {
+  static constexpr int NG = N / 4;
+  static constexpr int CG = 32 / NG;
+  static constexpr int WC = CPT * CG;
+  static constexpr int W = kDT / WC;
+  static constexpr int NT = 32 * W;
+};
 
 template <typename T, int N>
 struct FwdSmem {
@@ -34,7 +47,7 @@ struct FwdSmem {
   alignas(16) float dx_f[kTT * kDT];
   alignas(16) float B_f[kTT * N];
   alignas(16) float C_f[kTT * N];
-  alignas(16) float s_f[kTT * kDT];
+  alignas(16) float yp[kTT][N / 4][kDT + 8];  // per-lane shares of C_t . h_t over the lane's 4 states (row pitch spreads banks)
   alignas(16) float Dv_s[kDT];
   alignas(8) uint64_t full[kNST];
 };
@@ -49,23 +62,23 @@ struct FwdParams {
   int B, L, D, chunk, nchunks;
 };
 
-template <int N, typename T>
-__global__ void __launch_bounds__(Geo<N>::NT) scan_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
+template <int N, typename T, int CPT>
+__global__ void __launch_bounds__(GeoF<N, CPT>::NT) scan_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
                                                               const __grid_constant__ CUtensorMap tm_x,
                                                               const __grid_constant__ CUtensorMap tm_z,
                                                               const __grid_constant__ CUtensorMap tm_B,
                                                               const __grid_constant__ CUtensorMap tm_C) {
-  using G = Geo<N>;
+  using G = GeoF<N, CPT>;
   using AT = ActT<T>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   FwdSmem<T, N>& S = *reinterpret_cast<FwdSmem<T, N>*>(smem_raw);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ng = lane % G::NG, cg = lane / G::NG;
-  const int dl = warp * G::WC + cg * 2;  // first of the thread's two channels, CTA-local
+  const int dl = warp * G::WC + cg * CPT;  // first of the thread's channels, CTA-local
   const int d0 = blockIdx.x * kDT;
   const int dg = d0 + dl;
-  const bool dvalid = dg < p.D;  // D is a multiple of 8, so dg+1 < D as well
+  const bool dvalid = dg < p.D;  // D is a multiple of 8, so dg+CPT-1 < D as well
   const int n0 = ng * 4;
   const int L = p.L;
   const int ntiles = (L + kTT - 1) / kTT;
@@ -75,10 +88,10 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_fwd_kernel(const FwdParams p,
   constexpr uint32_t kBCBytes = kTT * N * AT::kBytes;
   constexpr uint32_t kStageBytes = 3 * kActBytes + 2 * kBCBytes;
 
-  // exponent scale A * log2(e) of the thread's 2 x 4 cells
-  float2 Ap[2][2];
+  // exponent scale A * log2(e) of the thread's CPT x 4 cells
+  float2 Ap[CPT][2];
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
+  for (int j = 0; j < CPT; ++j)
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       if (dvalid) {
@@ -110,7 +123,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_fwd_kernel(const FwdParams p,
   }
   __syncthreads();
 
-  float2 h[2][2];
+  float2 h[CPT][2];
   for (int k = 0; k < nitems; ++k) {
     const int slot = k % kNST;
     const int b = (int)blockIdx.y + (k / ntiles) * (int)gridDim.y;
@@ -119,7 +132,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_fwd_kernel(const FwdParams p,
 
     if (ti == 0) {  // entering batch row b: initial state
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+      for (int j = 0; j < CPT; ++j) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (p.h0 != nullptr && dvalid) v = *reinterpret_cast<const float4*>(p.h0 + ((size_t)b * p.D + dg + j) * N + n0);
         h[j][0] = f2(v.x, v.y);
@@ -139,18 +152,12 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_fwd_kernel(const FwdParams p,
     }
 
     // widen the tile to fp32: delta, delta*x, B, C
-    for (int gi = tid; gi < kTT * kDT / 8; gi += G::NT) {
-      float dv[8], xv[8];
-      AT::ld8(&S.dlt[slot][gi * 8], dv);
-      AT::ld8(&S.x[slot][gi * 8], xv);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) xv[e] *= dv[e];
-      float4* dst = reinterpret_cast<float4*>(&S.dlt_f[gi * 8]);
-      dst[0] = make_float4(dv[0], dv[1], dv[2], dv[3]);
-      dst[1] = make_float4(dv[4], dv[5], dv[6], dv[7]);
-      float4* dst2 = reinterpret_cast<float4*>(&S.dx_f[gi * 8]);
-      dst2[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
-      dst2[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+    for (int gi = tid; gi < kTT * kDT / 4; gi += G::NT) {
+      float dv[4], xv[4];
+      AT::ld4(&S.dlt[slot][gi * 4], dv);
+      AT::ld4(&S.x[slot][gi * 4], xv);
+      reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
+      reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(dv[0] * xv[0], dv[1] * xv[1], dv[2] * xv[2], dv[3] * xv[3]);
     }
     for (int gi = tid; gi < kTT * N / 4; gi += G::NT) {
       float bv[4], cv[4];
@@ -161,69 +168,94 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_fwd_kernel(const FwdParams p,
     }
     __syncthreads();
 
-    // checkpoint: the state entering step t0 (chunk is a multiple of the tile)
-    if (dvalid && (t0 % p.chunk) == 0) {
-      const int c = t0 / p.chunk;
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-        *reinterpret_cast<float4*>(p.ckpt + (((size_t)b * p.D + dg + j) * p.nchunks + c) * N + n0) =
-            make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
-    }
-
     // the recurrence over the tile's 16 steps (steps past L were zero-filled
     // by TMA: delta = 0 gives a = 1 and no input, so they leave h unchanged)
-#pragma unroll 4
-    for (int r = 0; r < kTT; ++r) {
-      const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[r * kDT + dl]);
-      const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * kDT + dl]);
-      const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
-      const float4 Cv = *reinterpret_cast<const float4*>(&S.C_f[r * N + n0]);
-      const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
-      const float2 C01 = f2(Cv.x, Cv.y), C23 = f2(Cv.z, Cv.w);
-      float yj[2];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float2 dj = bc2(j ? dd.y : dd.x);
-        const float2 xj = bc2(j ? xx.y : xx.x);
-        const float2 a0 = ex2_2(mul2(dj, Ap[j][0]));
-        const float2 a1 = ex2_2(mul2(dj, Ap[j][1]));
-        h[j][0] = fma2(a0, h[j][0], mul2(xj, B01));
-        h[j][1] = fma2(a1, h[j][1], mul2(xj, B23));
-        const float2 yy = fma2(C23, h[j][1], mul2(C01, h[j][0]));
-        yj[j] = yy.x + yy.y;
+    for (int half = 0; half < 2; ++half) {
+      constexpr int kH = kTT / 2;
+      // checkpoint: the state entering step t0 + 8 half (chunk is 8 or a multiple of the tile)
+      const int tc = t0 + half * kH;
+      if (dvalid && tc < L && (tc % p.chunk) == 0) {
+        const int c = tc / p.chunk;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j)
+          *reinterpret_cast<float4*>(p.ckpt + (((size_t)b * p.nchunks + c) * p.D + dg + j) * N + n0) =
+              make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
       }
-      // C_t . h_t across the NG lanes of the pair group
-      if constexpr (G::NG == 4) {
-        const bool up = ng & 2;
-        float keep = up ? yj[1] : yj[0];
-        keep += __shfl_xor_sync(0xffffffffu, up ? yj[0] : yj[1], 2);
-        keep += __shfl_xor_sync(0xffffffffu, keep, 1);
-        if ((ng & 1) == 0) S.s_f[r * kDT + dl + (ng >> 1)] = keep;
-      } else if constexpr (G::NG == 2) {
-        const bool up = ng & 1;
-        float keep = up ? yj[1] : yj[0];
-        keep += __shfl_xor_sync(0xffffffffu, up ? yj[0] : yj[1], 1);
-        S.s_f[r * kDT + dl + ng] = keep;
-      } else {
-        *reinterpret_cast<float2*>(&S.s_f[r * kDT + dl]) = f2(yj[0], yj[1]);
+      float2 av[kH][CPT][2];
+#pragma unroll
+      for (int i = 0; i < kH; ++i) {  // exponentials first: independent of the state
+        const int r = half * kH + i;
+        float dd[CPT];
+        if constexpr (CPT == 2) {
+          const float2 d2 = *reinterpret_cast<const float2*>(&S.dlt_f[r * kDT + dl]);
+          dd[0] = d2.x;
+          dd[CPT - 1] = d2.y;
+        } else {
+          dd[0] = S.dlt_f[r * kDT + dl];
+        }
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+          av[i][j][0] = ex2_2(mul2(bc2(dd[j]), Ap[j][0]));
+          av[i][j][1] = ex2_2(mul2(bc2(dd[j]), Ap[j][1]));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kH; ++i) {
+        const int r = half * kH + i;
+        float xx[CPT];
+        if constexpr (CPT == 2) {
+          const float2 x2 = *reinterpret_cast<const float2*>(&S.dx_f[r * kDT + dl]);
+          xx[0] = x2.x;
+          xx[CPT - 1] = x2.y;
+        } else {
+          xx[0] = S.dx_f[r * kDT + dl];
+        }
+        const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
+        const float4 Cv = *reinterpret_cast<const float4*>(&S.C_f[r * N + n0]);
+        const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
+        const float2 C01 = f2(Cv.x, Cv.y), C23 = f2(Cv.z, Cv.w);
+        float yj[CPT];
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+          const float2 xj = bc2(xx[j]);
+          h[j][0] = fma2(av[i][j][0], h[j][0], mul2(xj, B01));
+          h[j][1] = fma2(av[i][j][1], h[j][1], mul2(xj, B23));
+          const float2 yy = fma2(C23, h[j][1], mul2(C01, h[j][0]));
+          yj[j] = yy.x + yy.y;
+        }
+        // this lane's share of C_t . h_t; the NG shares are summed in the epilogue
+        if constexpr (CPT == 2) *reinterpret_cast<float2*>(&S.yp[r][ng][dl]) = f2(yj[0], yj[CPT - 1]);
+        else S.yp[r][ng][dl] = yj[0];
       }
     }
     __syncthreads();
 
-    // epilogue: y = (s + D x) * silu(z)
-    for (int gi = tid; gi < kTT * kDT / 8; gi += G::NT) {
-      const int r = gi / (kDT / 8), c8 = (gi % (kDT / 8)) * 8;
-      const int t = t0 + r, d = d0 + c8;
+    // epilogue: y = (s + D x) * silu(z), four channels per thread
+    for (int gi = tid; gi < kTT * kDT / 4; gi += G::NT) {
+      const int r = gi / (kDT / 4), c4 = (gi % (kDT / 4)) * 4;
+      const int t = t0 + r, d = d0 + c4;
       if (t < L && d < p.D) {
-        float xv[8], zv[8], o[8];
-        AT::ld8(&S.x[slot][r * kDT + c8], xv);
-        AT::ld8(&S.z[slot][r * kDT + c8], zv);
+        float xv[4], zv[4];
+        AT::ld4(&S.x[slot][r * kDT + c4], xv);
+        AT::ld4(&S.z[slot][r * kDT + c4], zv);
+        float4 sv = *reinterpret_cast<const float4*>(&S.yp[r][0][c4]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float s = S.s_f[r * kDT + c8 + e] + S.Dv_s[c8 + e] * xv[e];
-          o[e] = s * zv[e] * sigmoid(zv[e]);
+        for (int g = 1; g < N / 4; ++g) {
+          const float4 u = *reinterpret_cast<const float4*>(&S.yp[r][g][c4]);
+          sv.x += u.x; sv.y += u.y; sv.z += u.z; sv.w += u.w;
         }
-        AT::st8(reinterpret_cast<T*>(p.y) + ((size_t)b * L + t) * p.D + d, o);
+        const float4 Dd = *reinterpret_cast<const float4*>(&S.Dv_s[c4]);
+        const float s0 = fmaf(Dd.x, xv[0], sv.x), s1 = fmaf(Dd.y, xv[1], sv.y);
+        const float s2 = fmaf(Dd.z, xv[2], sv.z), s3 = fmaf(Dd.w, xv[3], sv.w);
+        T* out = reinterpret_cast<T*>(p.y) + ((size_t)b * L + t) * p.D + d;
+        const float o0 = s0 * zv[0] * sigmoid(zv[0]), o1 = s1 * zv[1] * sigmoid(zv[1]);
+        const float o2 = s2 * zv[2] * sigmoid(zv[2]), o3 = s3 * zv[3] * sigmoid(zv[3]);
+        if constexpr (sizeof(T) == 4) {
+          *reinterpret_cast<float4*>(out) = make_float4(o0, o1, o2, o3);
+        } else {
+          *reinterpret_cast<uint2*>(out) = make_uint2(ActT<__nv_bfloat16>::pack2(o0, o1), ActT<__nv_bfloat16>::pack2(o2, o3));
+        }
       }
     }
     __syncthreads();
@@ -231,14 +263,14 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_fwd_kernel(const FwdParams p,
 
     if (ti == ntiles - 1 && p.h_last != nullptr && dvalid) {
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
+      for (int j = 0; j < CPT; ++j)
         *reinterpret_cast<float4*>(p.h_last + ((size_t)b * p.D + dg + j) * N + n0) =
             make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
     }
   }
 }
 
-template <int N, typename T>
+template <int N, typename T, int CPT = 1>
 int launch_fwd(const FwdParams& p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z,
                cudaStream_t stream) {
   constexpr int e = ActT<T>::kBytes;
@@ -259,9 +291,9 @@ int launch_fwd(const FwdParams& p, const void* x, const void* delta, const void*
   const int cap = 1024 / ndt > 0 ? 1024 / ndt : 1;  // about 1024 CTAs; each loops over its batch rows
   const int gy = p.B < cap ? p.B : cap;
   const size_t smem = sizeof(FwdSmem<T, N>);
-  auto kern = scan_fwd_kernel<N, T>;
+  auto kern = scan_fwd_kernel<N, T, CPT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
-  kern<<<dim3(ndt, gy), Geo<N>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
+  kern<<<dim3(ndt, gy), GeoF<N, CPT>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
@@ -285,7 +317,7 @@ extern "C" int ss_scan_fwd(const void* x, const void* delta, const float* A, con
   if (B <= 0 || L <= 0 || D <= 0 || N <= 0 || chunk <= 0) return SS_ERR_DIM;
   if (N != 4 && N != 8 && N != 16) return SS_ERR_UNSUPPORTED;
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
-  if (chunk % kTT != 0) return SS_ERR_UNSUPPORTED;
+  if (chunk != kS && chunk % kTT != 0) return SS_ERR_UNSUPPORTED;
   if (D % 8 != 0) return SS_ERR_ALIGN;
   // the B_t / C_t rows of one batch element must span a multiple of 16 bytes (TMA stride rule)
   if (((long long)L * N * (dtype == SS_F32 ? 4 : 2)) % 16 != 0) return SS_ERR_ALIGN;

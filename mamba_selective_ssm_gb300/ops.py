@@ -76,7 +76,7 @@ def ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int = 64, want_h_las
         _req(h0, "h0", (B, D, N), torch.float32, dev)
     nck = num_chunks(L, chunk) if L > 0 and chunk > 0 else 0
     y = torch.empty_like(x)
-    ckpt = torch.empty((B, D, max(nck, 1), N), device=dev, dtype=torch.float32)
+    ckpt = torch.empty((B, max(nck, 1), D, N), device=dev, dtype=torch.float32)
     h_last = torch.empty((B, D, N), device=dev, dtype=torch.float32) if want_h_last else None
     rc = lib.ss_scan_fwd(_p(x), _p(delta), _p(A), _p(Bm), _p(Cm), _p(Dv), _p(z), _p(h0), _p(y), _p(ckpt), _p(h_last),
                          B, L, D, N, chunk, _DT[dt], _stream())
@@ -103,7 +103,7 @@ def ss_scan_bwd(x, delta, A, Bm, Cm, Dv, z, ckpt, dy, dh_last=None, chunk: int =
         _req(t, name, (B, L, N), dt, dev)
     _req(A, "A", (D, N), torch.float32, dev)
     _req(Dv, "Dv", (D,), torch.float32, dev)
-    _req(ckpt, "ckpt", (B, D, num_chunks(L, chunk), N), torch.float32, dev)
+    _req(ckpt, "ckpt", (B, num_chunks(L, chunk), D, N), torch.float32, dev)
     if dh_last is not None:
         _req(dh_last, "dh_last", (B, D, N), torch.float32, dev)
     f32 = dict(device=dev, dtype=torch.float32)

@@ -10,8 +10,8 @@ description "BPTT through SSM state"):
     y_t[d]   = s_t[d] * silu(z_t[d]),    silu(z) = z * sigmoid(z)
 
 Shapes: x, delta, z, y, dy: [B, L, D]; Bm, Cm: [B, L, N]; A: [D, N]; Dv: [D];
-h0, h_last: [B, D, N]; checkpoints [B, D, ceil(L/chunk), N] with
-ckpt[b, d, c, :] = the state just before step c*chunk (c = 0 holds h0 or zeros).
+h0, h_last: [B, D, N]; checkpoints [B, ceil(L/chunk), D, N] with
+ckpt[b, c, d, :] = the state just before step c*chunk (c = 0 holds h0 or zeros).
 
 Backward of the scalar loss sum(y * dy), by hand (reverse mode):
 
@@ -50,7 +50,7 @@ def _step(h: np.ndarray, delta_t: np.ndarray, x_t: np.ndarray, B_t: np.ndarray, 
 
 
 def scan_fwd_ref(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int | None = None):
-    """Forward scan. Returns (y [B,L,D], h_last [B,D,N], ckpt [B,D,ceil(L/chunk),N] or None)."""
+    """Forward scan. Returns (y [B,L,D], h_last [B,D,N], ckpt [B,ceil(L/chunk),D,N] or None)."""
     x, delta, z = (np.asarray(v, np.float64) for v in (x, delta, z))
     A, Bm, Cm, Dv = (np.asarray(v, np.float64) for v in (A, Bm, Cm, Dv))
     Bsz, L, D = x.shape
@@ -59,10 +59,10 @@ def scan_fwd_ref(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int | None = None):
     y = np.empty((Bsz, L, D))
     ckpt = None
     if chunk:
-        ckpt = np.empty((Bsz, D, -(-L // chunk), N))
+        ckpt = np.empty((Bsz, -(-L // chunk), D, N))
     for t in range(L):
         if chunk and t % chunk == 0:
-            ckpt[:, :, t // chunk, :] = h
+            ckpt[:, t // chunk] = h
         _, h = _step(h, delta[:, t], x[:, t], Bm[:, t], A)
         s = np.sum(h * Cm[:, t, None, :], axis=-1) + Dv[None, :] * x[:, t]
         y[:, t] = s * (z[:, t] * _sigmoid(z[:, t]))

@@ -32,6 +32,11 @@ CASES = [
     (2, 1, 8, 16, "f32", 16),       # L = 1
     (2, 130, 64, 16, "f32", 256),   # chunk longer than the sequence
     (4, 96, 128, 16, "bf16", 32),
+    # chunk = 8: a checkpoint per 8-step window, no recompute pass in the backward
+    (2, 100, 40, 16, "f32", 8),
+    (3, 77, 64, 8, "bf16", 8),
+    (1, 300, 136, 16, "bf16", 8),
+    (2, 5, 8, 4, "f32", 8),
 ]
 
 
@@ -62,9 +67,9 @@ def test_scan_parity(ss, B, L, D, N, dtype, chunk):
     assert ss.device_status() == 0
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_scan_h0_dh_last_and_accumulation(ss, dtype):
-    B, L, D, N, chunk = 2, 77, 48, 16, 32
+@pytest.mark.parametrize("dtype,chunk", [("f32", 32), ("bf16", 32), ("f32", 8)])
+def test_scan_h0_dh_last_and_accumulation(ss, dtype, chunk):
+    B, L, D, N = 2, 77, 48, 16
     wl = CONFIGS["tiny"].with_(B=B, L=L, D=D, N=N, dtype=dtype, chunk=chunk)
     inp = make_scan_inputs(wl, seed=7)
     rng = np.random.default_rng(3)

@@ -72,8 +72,8 @@ def test_fwd_matches_bidiagonal_solve():
             rhs[0] += a[0] * p["h0"][0, d, n]
             h = np.linalg.solve(M, rhs)
             assert abs(h[-1] - h_last[0, d, n]) <= 1e-12 * max(1.0, abs(h[-1]))
-            np.testing.assert_allclose(ckpt[0, d, 1:, n], h[:-1], rtol=1e-12, atol=1e-14)
-            assert ckpt[0, d, 0, n] == p["h0"][0, d, n]
+            np.testing.assert_allclose(ckpt[0, 1:, d, n], h[:-1], rtol=1e-12, atol=1e-14)
+            assert ckpt[0, 0, d, n] == p["h0"][0, d, n]
 
 
 def test_fwd_L1_closed_form():
@@ -96,7 +96,7 @@ def test_fwd_A_zero_is_cumsum():
     drive = (p["delta"] * p["x"])[..., None] * p["Bm"][:, :, None, :]  # [B,L,D,N]
     cs = np.cumsum(drive, axis=1) + p["h0"][:, None]
     np.testing.assert_allclose(h_last, cs[:, -1], rtol=1e-12, atol=1e-12)
-    np.testing.assert_allclose(ckpt[:, :, 1:, :], np.moveaxis(cs[:, 4:-1:5], 1, 2), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ckpt[:, 1:], cs[:, 4:-1:5], rtol=1e-12, atol=1e-12)
     p["A"] = np.full_like(p["A"], -1e-9)
     _, h_small, _ = _fwd(p)
     assert max_rel_err(h_small, cs[:, -1]) < 1e-7
@@ -145,15 +145,15 @@ def test_fwd_checkpoints_are_prefix_states():
     rng = np.random.default_rng(7)
     p = _rand_inputs(rng, B=2, L=13, D=2, N=2)
     _, _, ckpt = _fwd(p, chunk=4)
-    assert ckpt.shape == (2, 2, 4, 2)
-    np.testing.assert_array_equal(ckpt[:, :, 0], p["h0"])
+    assert ckpt.shape == (2, 4, 2, 2)
+    np.testing.assert_array_equal(ckpt[:, 0], p["h0"])
     for c in range(1, 4):
         q = {k: (v[:, : 4 * c] if k in ("x", "delta", "z", "Bm", "Cm", "dy") else v) for k, v in p.items()}
         _, hc, _ = _fwd(q)
-        np.testing.assert_array_equal(ckpt[:, :, c], hc)
+        np.testing.assert_array_equal(ckpt[:, c], hc)
     p["h0"] = None
     _, _, ck0 = _fwd(p, chunk=4)
-    assert np.all(ck0[:, :, 0] == 0)
+    assert np.all(ck0[:, 0] == 0)
 
 
 def test_fwd_C_zero_gives_skip_path():
