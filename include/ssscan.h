@@ -169,6 +169,33 @@ int rmsnorm_bwd(const void* dy, const void* x, const float* scale, const float* 
                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * rmsnorm_bwd_noalloc — rmsnorm_bwd for callers that cannot allocate device
+ * memory: code that runs under an allocator it does not own (a host
+ * framework's operator or plugin interface that hands over only inputs and
+ * outputs), or that cannot pay the device-wide synchronisation a cudaMalloc /
+ * cudaFree may cause in a latency-critical loop.  The pages have no
+ * counterpart of this entry point; it computes exactly what rmsnorm_bwd
+ * computes, with the same argument meaning, layout and errors, minus the
+ * workspace arguments.
+ *   - Scratch: a fixed array inside the library (4 MiB per GPU that loads the
+ *     library, held until the process exits) takes the per-block dscale
+ *     partials; nothing is allocated or freed by the call.
+ *   - Limit: dim <= 8192; larger dim returns SS_ERR_DIM before any launch.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array: calls that may overlap on the GPU
+ *     (other streams, other host threads) race on it and must be serialised
+ *     by the caller.  Each call overwrites every partial it reads, so no
+ *     clearing is needed.
+ *   - dscale partials are summed over a different number of blocks than in
+ *     rmsnorm_bwd, so dscale can differ from rmsnorm_bwd's in the last bits;
+ *     dx is identical.
+ */
+int rmsnorm_bwd_noalloc(const void* dy, const void* x, const float* scale, const float* rms,
+                        float* dx, float* dscale, int rows, int dim, int dtype, void* stream);
+
+/*
  * ss_device_status — synchronises `stream`, then reads and clears the
  * library's device-side error word.  Returns SS_OK, or SS_ERR_DEVICE when a
  * kernel gave up on a bounded wait for its own asynchronous copies since the

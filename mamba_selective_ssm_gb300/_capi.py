@@ -37,6 +37,7 @@ SIGNATURES = {
     "conv1d_causal_bwd": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _sz, _vp]),
     "rmsnorm_bwd_workspace_size": (_sz, [_i, _i]),
     "rmsnorm_bwd": (_i, [_vp] * 6 + [_i] * 3 + [_vp, _sz, _vp]),
+    "rmsnorm_bwd_noalloc": (_i, [_vp] * 6 + [_i] * 3 + [_vp]),
     "ss_device_status": (_i, [_vp]),
 }
 

@@ -10,7 +10,16 @@
 // (warp shuffles, then one shared-memory exchange whose buffer alternates
 // with the row parity, so one barrier per row suffices).  Per-CTA dscale
 // partials are added in fixed order by colsum_kernel.
+#include <mutex>
+
 #include "common.cuh"
+
+// Scratch of rmsnorm_bwd_noalloc: one dscale partial row per CTA of its fixed
+// 128-CTA grid, for dim up to 8192 (4 MiB).  Every GPU that loads the library
+// keeps this array until the process exits.
+constexpr int kNoAllocGrid = 128;
+constexpr int kNoAllocMaxDim = 8192;
+static __device__ __align__(256) float g_rms_noalloc_scratch[kNoAllocGrid * kNoAllocMaxDim];
 
 namespace {
 
@@ -160,6 +169,48 @@ extern "C" int rmsnorm_bwd(const void* dy, const void* x, const float* scale, co
   if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* ws = static_cast<float*>(workspace);
+  if (dtype == SS_F32) return rms_launch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+  return rms_launch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+}
+
+namespace {
+
+// Device address of g_rms_noalloc_scratch on the current device, looked up
+// once per device (in host code the array's name is only a stand-in).
+std::mutex g_noalloc_mu;
+constexpr int kMaxDevices = 64;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_rms_noalloc_scratch) != cudaSuccess || p == nullptr) return SS_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return SS_OK;
+}
+
+}  // namespace
+
+extern "C" int rmsnorm_bwd_noalloc(const void* dy, const void* x, const float* scale, const float* rms, float* dx,
+                                   float* dscale, int rows, int dim, int dtype, void* stream) {
+  if (!dy || !x || !scale || !rms || !dx || !dscale) return SS_ERR_NULL;
+  const int v = rms_validate(rows, dim, dtype);
+  if (v != SS_OK) return v;
+  if (dim > kNoAllocMaxDim) return SS_ERR_DIM;
+  const void* ptrs[] = {dy, x, scale, rms, dx, dscale};
+  for (const void* q : ptrs)
+    if (!ssh::aligned16(q)) return SS_ERR_ALIGN;
+  float* ws = nullptr;
+  const int rc = noalloc_scratch(&ws);
+  if (rc != SS_OK) return rc;
+  RmsPlan pl = rms_plan(rows, dim);
+  pl.grid = rows < kNoAllocGrid ? rows : kNoAllocGrid;  // every CTA overwrites its own partial row
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SS_F32) return rms_launch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
   return rms_launch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
 }
