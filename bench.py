@@ -176,12 +176,12 @@ def max_over_ranks(v, ws, device=None):
 
 # ---------------------------------------------------------------- oracle (CPU baseline / reference arm)
 
-def oracle_sample(wl, d_sample, seed=0):
-    """The float64 oracle on one batch row and the first d_sample channels of the workload."""
+def oracle_sample(wl, d_sample, seed=0, b_sample=1):
+    """The float64 oracle on b_sample batch rows and the first d_sample channels of the workload."""
     import numpy as np
     from oracle import conv1d_causal_bwd_ref, rmsnorm_bwd_ref, scan_bwd_ref, scan_fwd_ref
     from workloads import make_conv_inputs, make_rmsnorm_inputs, make_scan_inputs
-    sw = wl.with_(B=1, D=d_sample, d_model=max(8, d_sample // 2))
+    sw = wl.with_(B=b_sample, D=d_sample, d_model=max(8, d_sample // 2))
     inp = make_scan_inputs(sw, seed)
     cv = make_conv_inputs(sw, seed)
     rm = make_rmsnorm_inputs(sw, seed)
@@ -193,13 +193,16 @@ def oracle_sample(wl, d_sample, seed=0):
         conv1d_causal_bwd_ref(cv["dout"], cv["x"], cv["w"])
         rmsnorm_bwd_ref(rm["dy"], rm["x"], rm["scale"], rm["rms"])
 
-    return run, sw.B * sw.L * sw.D, f"B=1, L={sw.L}, D={d_sample}, N={sw.N} of the {wl.name} layer (scan fwd+bwd, " \
-                                    f"conv1d bwd, RMSNorm bwd [L, {sw.d_model}]), float64 NumPy"
+    return run, sw.B * sw.L * sw.D, f"B={b_sample}, L={sw.L}, D={d_sample}, N={sw.N} of the {wl.name} layer (scan fwd+bwd, " \
+                                    f"conv1d bwd, RMSNorm bwd [B*L, {sw.d_model}]), float64 NumPy"
 
 
-def cpu_baseline(wl, d_sample=2048):
+def cpu_baseline(wl, d_sample=None, b_sample=None):
+    """About 10-15 s of one host core on a slice of the workload (3 of 4 rows x all channels for the 1.4B layer)."""
     os.environ.setdefault("OMP_NUM_THREADS", "1")
-    run, elems, desc = oracle_sample(wl, d_sample)
+    d_sample = d_sample or min(wl.D, 4096)
+    b_sample = b_sample or max(1, min(wl.B - 1, (3 * 2048 * 4096) // (wl.L * d_sample)))
+    run, elems, desc = oracle_sample(wl, d_sample, b_sample=b_sample)
     t = time.perf_counter()
     run()
     dt = time.perf_counter() - t

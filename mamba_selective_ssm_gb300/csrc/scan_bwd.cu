@@ -2,7 +2,7 @@
 // time through the diagonal SSM state, with the states rebuilt from the
 // forward's chunk checkpoints instead of a stored [B, L, D, N] history.
 //
-// One CTA = 64 channels of one batch row at a time.  Chunks are visited from
+// One CTA = 32 channels (64 when N = 4) of one batch row at a time.  Chunks are visited from
 // last to first; each chunk (a multiple of 16 steps) is walked twice:
 //   pass A (tiles in order):   from the chunk's checkpoint, advance
 //       h_t = a_t h_{t-1} + delta_t B_t x_t and park the state entering every
@@ -18,7 +18,7 @@
 // shares to shared memory; the window epilogue adds the shares in a fixed
 // order (over the 4-state lane groups for the per-(t,d) sums, over lanes and
 // warps for dB_t, dC_t) and writes dx, ddelta, dz and one dB/dC partial per
-// 64-channel tile.  ss_bwd_dbc_kernel and colsum_kernel add the partials of
+// channel tile.  ss_bwd_dbc_kernel and colsum_kernel add the partials of
 // dB/dC and of dA/dD in fixed order.  No atomics: results are bitwise
 // reproducible.
 #include "scan_common.cuh"
@@ -29,21 +29,27 @@ using namespace ssk;
 
 __device__ unsigned g_bwd_err;
 
-constexpr int kSP = kDT + 8;        // row pitch of the C.h shares (bank spread across lane groups)
-constexpr int kSAB = 2 * kDT + 8;   // row pitch of the (sum qA, sum GB) shares
+// Channels per CTA: 32 (two warps at N = 16) so that a Mamba-sized layer has
+// enough CTAs to keep ~4 per SM; N = 4 needs 64 (one warp spans 64 channels).
+template <int N>
+constexpr int bwd_dt() {
+  return Geo<N, 64>::WC > 32 ? 64 : 32;
+}
 
-template <typename T, int N, int NSTG>
+template <typename T, int N, int NSTG, int DT>
 struct BwdSmem {
-  static constexpr int W = Geo<N>::W, CG = Geo<N>::CG;
-  alignas(128) T dlt[NSTG][kTT * kDT];
-  alignas(128) T x[NSTG][kTT * kDT];
-  alignas(128) T z[NSTG][kTT * kDT];
-  alignas(128) T dy[NSTG][kTT * kDT];
+  static constexpr int W = Geo<N, DT>::W, CG = Geo<N, DT>::CG;
+  static constexpr int kSP = DT + 8;       // row pitch of the C.h shares (bank spread across lane groups)
+  static constexpr int kSAB = 2 * DT + 8;  // row pitch of the (sum qA, sum GB) shares
+  alignas(128) T dlt[NSTG][kTT * DT];
+  alignas(128) T x[NSTG][kTT * DT];
+  alignas(128) T z[NSTG][kTT * DT];
+  alignas(128) T dy[NSTG][kTT * DT];
   alignas(128) T Bm[NSTG][kTT * N];
   alignas(128) T Cm[NSTG][kTT * N];
-  alignas(16) float dlt_f[kTT * kDT];
-  alignas(16) float dx_f[kTT * kDT];  // delta * x
-  alignas(16) float ds_f[kTT * kDT];  // dy * silu(z)
+  alignas(16) float dlt_f[kTT * DT];
+  alignas(16) float dx_f[kTT * DT];  // delta * x
+  alignas(16) float ds_f[kTT * DT];  // dy * silu(z)
   alignas(16) float B_f[kTT * N];
   alignas(16) float C_f[kTT * N];
   // one 8-step window's per-lane shares
@@ -52,7 +58,7 @@ struct BwdSmem {
   // [warp][step][dB | dC][channel-pair group x state]: G_t delta_t x_t and ds_t h_t summed over
   // the lane's 2 channels (row pitch CG*N + 16 keeps the epilogue's 128-bit reads conflict-free)
   alignas(16) float dbc[W][kS][2][CG * N + 16];
-  alignas(16) float Dv_s[kDT];
+  alignas(16) float Dv_s[DT];
   alignas(8) uint64_t full[NSTG];
   uint32_t tmem_base;
 };
@@ -74,28 +80,28 @@ struct BwdParams {
   float* ddelta;
   float* dz;
   float* dh0;
-  float* ws_dBC;  // [ndt][B][L][2N]
+  float* ws_dBC;  // [channel tiles][B][L][2N]
   float* ws_dAD;  // [gy][D*N + D]: dA then dD partials of each CTA row
   int B, L, D, chunk, nchunks;
   uint32_t tcols;
 };
 
-template <int N, typename T, int NSTG>
-__global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
+template <int N, typename T, int NSTG, int DT>
+__global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
                                                               const __grid_constant__ CUtensorMap tm_x,
                                                               const __grid_constant__ CUtensorMap tm_z,
                                                               const __grid_constant__ CUtensorMap tm_dy,
                                                               const __grid_constant__ CUtensorMap tm_B,
                                                               const __grid_constant__ CUtensorMap tm_C) {
-  using G = Geo<N>;
+  using G = Geo<N, DT>;
   using AT = ActT<T>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  BwdSmem<T, N, NSTG>& S = *reinterpret_cast<BwdSmem<T, N, NSTG>*>(smem_raw);
+  BwdSmem<T, N, NSTG, DT>& S = *reinterpret_cast<BwdSmem<T, N, NSTG, DT>*>(smem_raw);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ng = lane % G::NG, cg = lane / G::NG;
   const int dl = warp * G::WC + cg * 2;
-  const int d0 = blockIdx.x * kDT;
+  const int d0 = blockIdx.x * DT;
   const int dg = d0 + dl;
   const bool dvalid = dg < p.D;
   const int n0 = ng * 4;
@@ -107,7 +113,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
   const int per_b = direct ? ntiles : 2 * ntiles;       // items per batch row
   const int nb = (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
   const int nitems = nb * per_b;
-  constexpr uint32_t kActBytes = kTT * kDT * AT::kBytes;
+  constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
   constexpr uint32_t kBCBytes = kTT * N * AT::kBytes;
 
   float2 Ap[2][2];
@@ -122,7 +128,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
         Ap[j][q] = f2(0.f, 0.f);
       }
     }
-  for (int c = tid; c < kDT; c += G::NT) S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
+  for (int c = tid; c < DT; c += G::NT) S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
 
   // item k -> (batch row, tile of the sequence, pass; lastA: last pass-A tile of its chunk)
   auto decode = [&](int k, int& b, int& gt, bool& passB, bool& lastA) {
@@ -168,7 +174,10 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
     }
   };
 
-  if (warp == 0 && !direct) tmem_alloc(&S.tmem_base, p.tcols);
+  if (warp == 0) {
+    if (!direct) tmem_alloc(&S.tmem_base, p.tcols);
+    tmem_relinquish();
+  }
   if (tid == 0) {
     prefetch_tmap(&tm_dlt); prefetch_tmap(&tm_x); prefetch_tmap(&tm_z);
     prefetch_tmap(&tm_dy); prefetch_tmap(&tm_B); prefetch_tmap(&tm_C);
@@ -234,7 +243,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
           h[j][1] = f2(v.z, v.w);
         }
       }
-      for (int gi = tid; gi < kTT * kDT / 4; gi += G::NT) {
+      for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
         float dv[4], xv[4];
         AT::ld4(&S.dlt[slot][gi * 4], dv);
         AT::ld4(&S.x[slot][gi * 4], xv);
@@ -255,7 +264,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
         float2 av[kS][2][2];
 #pragma unroll
         for (int i = 0; i < kS; ++i) {  // exponentials first: independent of the state
-          const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[(half * kS + i) * kDT + dl]);
+          const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[(half * kS + i) * DT + dl]);
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const float2 dj = bc2(j ? dd.y : dd.x);
@@ -266,7 +275,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
 #pragma unroll
         for (int i = 0; i < kS; ++i) {
           const int r = half * kS + i;
-          const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * kDT + dl]);
+          const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * DT + dl]);
           const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
           const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
 #pragma unroll
@@ -296,7 +305,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    for (int gi = tid; gi < kTT * kDT / 4; gi += G::NT) {
+    for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
       float dv[4], xv[4], zv[4], gv[4];
       AT::ld4(&S.dlt[slot][gi * 4], dv);
       AT::ld4(&S.x[slot][gi * 4], xv);
@@ -337,7 +346,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
       float2 av[kS][2][2], hv[kS][2][2];
 #pragma unroll
       for (int i = 0; i < kS; ++i) {  // exponentials first: independent of the state
-        const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[(sub * kS + i) * kDT + dl]);
+        const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[(sub * kS + i) * DT + dl]);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const float2 dj = bc2(j ? dd.y : dd.x);
@@ -349,8 +358,8 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
 #pragma unroll
       for (int i = 0; i < kS; ++i) {
         const int r = sub * kS + i;
-        const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * kDT + dl]);
-        const float2 gg = *reinterpret_cast<const float2*>(&S.ds_f[r * kDT + dl]);
+        const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * DT + dl]);
+        const float2 gg = *reinterpret_cast<const float2*>(&S.ds_f[r * DT + dl]);
         const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
         const float4 Cv = *reinterpret_cast<const float4*>(&S.C_f[r * N + n0]);
         const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
@@ -382,9 +391,9 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
 #pragma unroll
       for (int i = kS - 1; i >= 0; --i) {
         const int r = sub * kS + i;
-        const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[r * kDT + dl]);
-        const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * kDT + dl]);
-        const float2 gg = *reinterpret_cast<const float2*>(&S.ds_f[r * kDT + dl]);
+        const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[r * DT + dl]);
+        const float2 xx = *reinterpret_cast<const float2*>(&S.dx_f[r * DT + dl]);
+        const float2 gg = *reinterpret_cast<const float2*>(&S.ds_f[r * DT + dl]);
         const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
         const float4 Cv = *reinterpret_cast<const float4*>(&S.C_f[r * N + n0]);
         const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
@@ -439,16 +448,16 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
           *reinterpret_cast<float4*>(&p.ws_dBC[(((size_t)blockIdx.x * p.B + b) * L + t) * (2 * N) + qq * N + n4]) = acc;
       }
       // per-(t, d) gradients, four channels per thread
-      for (int gi = tid; gi < kS * kDT / 4; gi += G::NT) {
-        const int i = gi / (kDT / 4), c4 = (gi % (kDT / 4)) * 4;
+      for (int gi = tid; gi < kS * DT / 4; gi += G::NT) {
+        const int i = gi / (DT / 4), c4 = (gi % (DT / 4)) * 4;
         const int rr = sub * kS + i;
         const int t = t0 + rr, d = d0 + c4;
         if (t < L && d < p.D) {
           float dv[4], xv[4], zv[4], gv[4], o0[4], o1[4], o2[4];
-          AT::ld4(&S.dlt[slot][rr * kDT + c4], dv);
-          AT::ld4(&S.x[slot][rr * kDT + c4], xv);
-          AT::ld4(&S.z[slot][rr * kDT + c4], zv);
-          AT::ld4(&S.dy[slot][rr * kDT + c4], gv);
+          AT::ld4(&S.dlt[slot][rr * DT + c4], dv);
+          AT::ld4(&S.x[slot][rr * DT + c4], xv);
+          AT::ld4(&S.z[slot][rr * DT + c4], zv);
+          AT::ld4(&S.dy[slot][rr * DT + c4], gv);
           float4 sv = *reinterpret_cast<const float4*>(&S.sp[i][0][c4]);
           float4 ab0 = *reinterpret_cast<const float4*>(&S.sab[i][0][2 * c4]);
           float4 ab1 = *reinterpret_cast<const float4*>(&S.sab[i][0][2 * c4 + 4]);
@@ -461,7 +470,7 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
             ab0.x += v0.x; ab0.y += v0.y; ab0.z += v0.z; ab0.w += v0.w;
             ab1.x += v1.x; ab1.y += v1.y; ab1.z += v1.z; ab1.w += v1.w;
           }
-          const float4 dsv = *reinterpret_cast<const float4*>(&S.ds_f[rr * kDT + c4]);
+          const float4 dsv = *reinterpret_cast<const float4*>(&S.ds_f[rr * DT + c4]);
           const float4 Dd4 = *reinterpret_cast<const float4*>(&S.Dv_s[c4]);
           const float shv[4] = {sv.x, sv.y, sv.z, sv.w};
           const float sAv[4] = {ab0.x, ab0.z, ab1.x, ab1.z};
@@ -514,11 +523,11 @@ __global__ void __launch_bounds__(Geo<N>::NT) scan_bwd_kernel(const BwdParams p,
   float* red = &S.sab[0][0][0];  // free after the last window
   *reinterpret_cast<float4*>(&red[tid * 4]) = make_float4(dDacc[0], dDacc[1], dDacc[2], dDacc[3]);
   __syncthreads();
-  for (int c = tid; c < kDT; c += G::NT) {
+  for (int c = tid; c < DT; c += G::NT) {
     if (d0 + c < p.D) {
       const int grp = c / 4, e = c % 4;
       float acc = 0.f;
-      for (int m = grp; m < G::NT; m += kDT / 4) acc += red[m * 4 + e];
+      for (int m = grp; m < G::NT; m += DT / 4) acc += red[m * 4 + e];
       p.ws_dAD[(size_t)blockIdx.y * p.D * (N + 1) + (size_t)p.D * N + d0 + c] = acc;
     }
   }
@@ -555,7 +564,8 @@ struct BwdPlan {
 
 inline BwdPlan make_plan(int B, int L, int D, int N) {
   BwdPlan pl;
-  pl.ndt = (D + kDT - 1) / kDT;
+  const int dt = N == 4 ? bwd_dt<4>() : N == 8 ? bwd_dt<8>() : bwd_dt<16>();
+  pl.ndt = (D + dt - 1) / dt;
   const int cap = 1024 / pl.ndt > 0 ? 1024 / pl.ndt : 1;
   pl.gy = B < cap ? B : cap;
   const size_t bc = (size_t)pl.ndt * B * L * 2 * N * sizeof(float);
@@ -570,7 +580,7 @@ struct Stages {
   static constexpr int value = sizeof(T) == 4 ? 2 : 3;
 };
 
-template <int N, typename T, int NSTG = Stages<T>::value>
+template <int N, typename T, int NSTG = Stages<T>::value, int DT = bwd_dt<N>()>
 int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, const void* dy,
                float* dA, float* dB, float* dC, float* dD, void* ws, cudaStream_t stream) {
   constexpr int e = ActT<T>::kBytes;
@@ -581,7 +591,7 @@ int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, co
   CUtensorMap tm[6];
   const uint64_t adims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
   const uint64_t astr[2] = {(uint64_t)p.D * e, (uint64_t)p.L * p.D * e};
-  const uint32_t abox[3] = {kDT, kTT, 1};
+  const uint32_t abox[3] = {DT, kTT, 1};
   const uint64_t bdims[2] = {(uint64_t)p.L * N, (uint64_t)p.B};
   const uint64_t bstr[1] = {(uint64_t)p.L * N * e};
   const uint32_t bbox[2] = {kTT * N, 1};
@@ -592,15 +602,15 @@ int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, co
       !ssh::encode_tiled(&tm[4], ActT<T>::kTma, 2, Bm, bdims, bstr, bbox) ||
       !ssh::encode_tiled(&tm[5], ActT<T>::kTma, 2, Cm, bdims, bstr, bbox))
     return SS_ERR_CUDA;
-  const size_t smem = sizeof(BwdSmem<T, N, NSTG>);
-  auto kern = scan_bwd_kernel<N, T, NSTG>;
+  const size_t smem = sizeof(BwdSmem<T, N, NSTG, DT>);
+  auto kern = scan_bwd_kernel<N, T, NSTG, DT>;
   // TMEM: the CTAs resident on one SM must fit in its 512 columns, else an
   // allocation would wait for another CTA to finish.  Ask for enough shared
   // memory per CTA to keep the residency within that bound.
   size_t smem_launch = smem;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Geo<N>::NT, smem) != cudaSuccess) return SS_ERR_CUDA;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Geo<N, DT>::NT, smem) != cudaSuccess) return SS_ERR_CUDA;
   if (p.tcols != 0 && (uint32_t)per_sm * p.tcols > 512u) {
     const int max_ctas = 512 / (int)p.tcols;
     smem_launch = (size_t)(227 * 1024) / (size_t)(max_ctas + 1) + 1024;
@@ -608,11 +618,11 @@ int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, co
     if (smem_launch > 227 * 1024) smem_launch = 227 * 1024;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_launch) != cudaSuccess)
       return SS_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Geo<N>::NT, smem_launch) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Geo<N, DT>::NT, smem_launch) != cudaSuccess)
       return SS_ERR_CUDA;
     if ((uint32_t)per_sm * p.tcols > 512u) return SS_ERR_UNSUPPORTED;
   }
-  kern<<<dim3(pl.ndt, pl.gy), Geo<N>::NT, smem_launch, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4], tm[5]);
+  kern<<<dim3(pl.ndt, pl.gy), Geo<N, DT>::NT, smem_launch, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4], tm[5]);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
   const long long nBC = (long long)p.B * p.L * 2 * N;
   long long blocks = (nBC + 255) / 256;

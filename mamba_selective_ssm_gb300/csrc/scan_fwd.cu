@@ -2,7 +2,7 @@
 //
 //   h_t = exp(delta_t * A) * h_{t-1} + delta_t * B_t * x_t,   y_t = (C_t . h_t + D x_t) * silu(z_t)
 //
-// One CTA = 64 channels of one batch row; the sequence is walked once, in
+// One CTA = 32 channels of one batch row; the sequence is walked once, in
 // order, 16 steps per TMA tile, with the N-state recurrences of every channel
 // held in registers (2 channels x 4 states per thread, f32x2-packed).  The
 // exponent uses one ex2 per (t, d, n) with A pre-scaled by log2 e.  Per tile:
@@ -27,28 +27,31 @@ constexpr int kNST = 4;  // TMA pipeline depth (tiles in flight)
 // Forward geometry: CPT channels x 4 states per thread (CPT = 1 doubles the
 // warps per SM relative to the backward's 2 x 4 cells, which the forward can
 // afford because it keeps no per-step history).
-template <int N, int CPT>
+template <int N, int CPT, int DT>
 struct GeoF {
   static constexpr int NG = N / 4;
   static constexpr int CG = 32 / NG;
   static constexpr int WC = CPT * CG;
-  static constexpr int W = kDT / WC;
+  static constexpr int W = DT / WC;
   static constexpr int NT = 32 * W;
+  static_assert(W >= 1 && DT % WC == 0, "a CTA holds whole warps");
 };
 
-template <typename T, int N>
+constexpr int kFDT = 32;  // channels per forward CTA
+
+template <typename T, int N, int DT>
 struct FwdSmem {
-  alignas(128) T dlt[kNST][kTT * kDT];
-  alignas(128) T x[kNST][kTT * kDT];
-  alignas(128) T z[kNST][kTT * kDT];
+  alignas(128) T dlt[kNST][kTT * DT];
+  alignas(128) T x[kNST][kTT * DT];
+  alignas(128) T z[kNST][kTT * DT];
   alignas(128) T Bm[kNST][kTT * N];
   alignas(128) T Cm[kNST][kTT * N];
-  alignas(16) float dlt_f[kTT * kDT];
-  alignas(16) float dx_f[kTT * kDT];
+  alignas(16) float dlt_f[kTT * DT];
+  alignas(16) float dx_f[kTT * DT];
   alignas(16) float B_f[kTT * N];
   alignas(16) float C_f[kTT * N];
-  alignas(16) float yp[kTT][N / 4][kDT + 8];  // per-lane shares of C_t . h_t over the lane's 4 states (row pitch spreads banks)
-  alignas(16) float Dv_s[kDT];
+  alignas(16) float yp[kTT][N / 4][DT + 8];  // per-lane shares of C_t . h_t over the lane's 4 states (row pitch spreads banks)
+  alignas(16) float Dv_s[DT];
   alignas(8) uint64_t full[kNST];
 };
 
@@ -62,21 +65,21 @@ struct FwdParams {
   int B, L, D, chunk, nchunks;
 };
 
-template <int N, typename T, int CPT>
-__global__ void __launch_bounds__(GeoF<N, CPT>::NT) scan_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
+template <int N, typename T, int CPT, int DT>
+__global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
                                                               const __grid_constant__ CUtensorMap tm_x,
                                                               const __grid_constant__ CUtensorMap tm_z,
                                                               const __grid_constant__ CUtensorMap tm_B,
                                                               const __grid_constant__ CUtensorMap tm_C) {
-  using G = GeoF<N, CPT>;
+  using G = GeoF<N, CPT, DT>;
   using AT = ActT<T>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  FwdSmem<T, N>& S = *reinterpret_cast<FwdSmem<T, N>*>(smem_raw);
+  FwdSmem<T, N, DT>& S = *reinterpret_cast<FwdSmem<T, N, DT>*>(smem_raw);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ng = lane % G::NG, cg = lane / G::NG;
   const int dl = warp * G::WC + cg * CPT;  // first of the thread's channels, CTA-local
-  const int d0 = blockIdx.x * kDT;
+  const int d0 = blockIdx.x * DT;
   const int dg = d0 + dl;
   const bool dvalid = dg < p.D;  // D is a multiple of 8, so dg+CPT-1 < D as well
   const int n0 = ng * 4;
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT>::NT) scan_fwd_kernel(const FwdPar
   const int ntiles = (L + kTT - 1) / kTT;
   const int nb = (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;  // batch rows of this CTA
   const int nitems = nb * ntiles;
-  constexpr uint32_t kActBytes = kTT * kDT * AT::kBytes;
+  constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
   constexpr uint32_t kBCBytes = kTT * N * AT::kBytes;
   constexpr uint32_t kStageBytes = 3 * kActBytes + 2 * kBCBytes;
 
@@ -101,7 +104,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT>::NT) scan_fwd_kernel(const FwdPar
         Ap[j][q] = f2(0.f, 0.f);
       }
     }
-  for (int c = tid; c < kDT; c += G::NT) S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
+  for (int c = tid; c < DT; c += G::NT) S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
 
   auto issue = [&](int k) {
     const int slot = k % kNST;
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT>::NT) scan_fwd_kernel(const FwdPar
     }
 
     // widen the tile to fp32: delta, delta*x, B, C
-    for (int gi = tid; gi < kTT * kDT / 4; gi += G::NT) {
+    for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
       float dv[4], xv[4];
       AT::ld4(&S.dlt[slot][gi * 4], dv);
       AT::ld4(&S.x[slot][gi * 4], xv);
@@ -186,31 +189,16 @@ __global__ void __launch_bounds__(GeoF<N, CPT>::NT) scan_fwd_kernel(const FwdPar
 #pragma unroll
       for (int i = 0; i < kH; ++i) {  // exponentials first: independent of the state
         const int r = half * kH + i;
-        float dd[CPT];
-        if constexpr (CPT == 2) {
-          const float2 d2 = *reinterpret_cast<const float2*>(&S.dlt_f[r * kDT + dl]);
-          dd[0] = d2.x;
-          dd[CPT - 1] = d2.y;
-        } else {
-          dd[0] = S.dlt_f[r * kDT + dl];
-        }
 #pragma unroll
         for (int j = 0; j < CPT; ++j) {
-          av[i][j][0] = ex2_2(mul2(bc2(dd[j]), Ap[j][0]));
-          av[i][j][1] = ex2_2(mul2(bc2(dd[j]), Ap[j][1]));
+          const float2 dj = bc2(S.dlt_f[r * DT + dl + j]);
+          av[i][j][0] = ex2_2(mul2(dj, Ap[j][0]));
+          av[i][j][1] = ex2_2(mul2(dj, Ap[j][1]));
         }
       }
 #pragma unroll
       for (int i = 0; i < kH; ++i) {
         const int r = half * kH + i;
-        float xx[CPT];
-        if constexpr (CPT == 2) {
-          const float2 x2 = *reinterpret_cast<const float2*>(&S.dx_f[r * kDT + dl]);
-          xx[0] = x2.x;
-          xx[CPT - 1] = x2.y;
-        } else {
-          xx[0] = S.dx_f[r * kDT + dl];
-        }
         const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
         const float4 Cv = *reinterpret_cast<const float4*>(&S.C_f[r * N + n0]);
         const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
@@ -218,7 +206,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT>::NT) scan_fwd_kernel(const FwdPar
         float yj[CPT];
 #pragma unroll
         for (int j = 0; j < CPT; ++j) {
-          const float2 xj = bc2(xx[j]);
+          const float2 xj = bc2(S.dx_f[r * DT + dl + j]);
           h[j][0] = fma2(av[i][j][0], h[j][0], mul2(xj, B01));
           h[j][1] = fma2(av[i][j][1], h[j][1], mul2(xj, B23));
           const float2 yy = fma2(C23, h[j][1], mul2(C01, h[j][0]));
@@ -232,13 +220,13 @@ __global__ void __launch_bounds__(GeoF<N, CPT>::NT) scan_fwd_kernel(const FwdPar
     __syncthreads();
 
     // epilogue: y = (s + D x) * silu(z), four channels per thread
-    for (int gi = tid; gi < kTT * kDT / 4; gi += G::NT) {
-      const int r = gi / (kDT / 4), c4 = (gi % (kDT / 4)) * 4;
+    for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
+      const int r = gi / (DT / 4), c4 = (gi % (DT / 4)) * 4;
       const int t = t0 + r, d = d0 + c4;
       if (t < L && d < p.D) {
         float xv[4], zv[4];
-        AT::ld4(&S.x[slot][r * kDT + c4], xv);
-        AT::ld4(&S.z[slot][r * kDT + c4], zv);
+        AT::ld4(&S.x[slot][r * DT + c4], xv);
+        AT::ld4(&S.z[slot][r * DT + c4], zv);
         float4 sv = *reinterpret_cast<const float4*>(&S.yp[r][0][c4]);
 #pragma unroll
         for (int g = 1; g < N / 4; ++g) {
@@ -270,14 +258,14 @@ __global__ void __launch_bounds__(GeoF<N, CPT>::NT) scan_fwd_kernel(const FwdPar
   }
 }
 
-template <int N, typename T, int CPT = 1>
+template <int N, typename T, int CPT = 1, int DT = kFDT>
 int launch_fwd(const FwdParams& p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z,
                cudaStream_t stream) {
   constexpr int e = ActT<T>::kBytes;
   CUtensorMap tm[5];
   const uint64_t adims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
   const uint64_t astr[2] = {(uint64_t)p.D * e, (uint64_t)p.L * p.D * e};
-  const uint32_t abox[3] = {kDT, kTT, 1};
+  const uint32_t abox[3] = {DT, kTT, 1};
   const uint64_t bdims[2] = {(uint64_t)p.L * N, (uint64_t)p.B};
   const uint64_t bstr[1] = {(uint64_t)p.L * N * e};
   const uint32_t bbox[2] = {kTT * N, 1};
@@ -287,13 +275,13 @@ int launch_fwd(const FwdParams& p, const void* x, const void* delta, const void*
       !ssh::encode_tiled(&tm[3], ActT<T>::kTma, 2, Bm, bdims, bstr, bbox) ||
       !ssh::encode_tiled(&tm[4], ActT<T>::kTma, 2, Cm, bdims, bstr, bbox))
     return SS_ERR_CUDA;
-  const int ndt = (p.D + kDT - 1) / kDT;
+  const int ndt = (p.D + DT - 1) / DT;
   const int cap = 1024 / ndt > 0 ? 1024 / ndt : 1;  // about 1024 CTAs; each loops over its batch rows
   const int gy = p.B < cap ? p.B : cap;
-  const size_t smem = sizeof(FwdSmem<T, N>);
-  auto kern = scan_fwd_kernel<N, T, CPT>;
+  const size_t smem = sizeof(FwdSmem<T, N, DT>);
+  auto kern = scan_fwd_kernel<N, T, CPT, DT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
-  kern<<<dim3(ndt, gy), GeoF<N, CPT>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
+  kern<<<dim3(ndt, gy), GeoF<N, CPT, DT>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 

@@ -62,9 +62,9 @@ class Workload:
 CONFIGS = {
     "tiny": Workload("tiny", 2, 64, 16, 4, 4, 8, "f32", 1e-3, 1e-1, 64,
                      "tiny fp32 scan fwd+bwd: B=2, L=64, d_inner=16, N=4, d_conv=4"),
-    "mamba130m": Workload("mamba130m", 8, 2048, 1536, 16, 4, 768, "f32", 1e-3, 1e-1, 64,
+    "mamba130m": Workload("mamba130m", 8, 2048, 1536, 16, 4, 768, "f32", 1e-3, 1e-1, 8,
                           "Mamba-130M-shaped layer: B=8, L=2048, d_model=768, d_inner=1536, N=16, fp32"),
-    "mamba1p4b": Workload("mamba1p4b", 4, 2048, 4096, 16, 4, 2048, "bf16", 1e-3, 1e-1, 64,
+    "mamba1p4b": Workload("mamba1p4b", 4, 2048, 4096, 16, 4, 2048, "bf16", 1e-3, 1e-1, 8,
                           "Mamba-1.4B-shaped layer: B=4, L=2048, d_model=2048, d_inner=4096, N=16, "
                           "bf16 x/delta/B/C/z/dy, fp32 state and grads"),
     "short": Workload("short", 4096, 32, 64, 16, 4, 32, "f32", 1e-3, 1e-1, 32,
