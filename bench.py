@@ -292,7 +292,7 @@ def main():
         "c_dx": torch.empty((B, L, D), **f32), "c_dw": torch.zeros((D, K), **f32), "c_db": torch.zeros((D,), **f32),
         "r_dx": torch.empty((B * L, H), **f32), "r_dscale": torch.zeros((H,), **f32),
     }
-    ws_scan = lib.ss_scan_bwd_workspace_size(B, L, D, N, chunk, sdt)
+    ws_scan = max(lib.ss_scan_bwd_workspace_size(B, L, D, N, chunk, sdt), lib.ss_scan_fwd_workspace_size(B, L, D, N, chunk, sdt))
     ws_conv = lib.conv1d_causal_bwd_workspace_size(B, L, D, K)
     ws_rms = lib.rmsnorm_bwd_workspace_size(B * L, H)
     W = torch.empty(max(ws_scan, ws_conv, ws_rms), device=dev, dtype=torch.uint8)
@@ -304,7 +304,7 @@ def main():
     calls = {
         "scan_fwd": lambda: lib.ss_scan_fwd(p(X["x"]), p(X["delta"]), p(X["A"]), p(X["Bm"]), p(X["Cm"]), p(X["Dv"]),
                                             p(X["z"]), None, p(O["y"]), p(O["ckpt"]), p(O["h_last"]),
-                                            B, L, D, N, chunk, sdt, sp),
+                                            B, L, D, N, chunk, sdt, p(W), wsz, sp),
         "scan_bwd": lambda: lib.ss_scan_bwd(p(X["x"]), p(X["delta"]), p(X["A"]), p(X["Bm"]), p(X["Cm"]), p(X["Dv"]),
                                             p(X["z"]), p(O["ckpt"]), p(X["dy"]), None, p(O["dx"]), p(O["ddelta"]),
                                             p(O["dz"]), p(O["dA"]), p(O["dB"]), p(O["dC"]), p(O["dD"]), p(O["dh0"]),

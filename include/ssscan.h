@@ -60,6 +60,12 @@ const char* ss_strerror(int code);
 int ss_scan_num_chunks(int L, int chunk);
 
 /*
+ * Workspace bytes ss_scan_fwd needs for these sizes (0 on invalid sizes, and
+ * 0 when the layer has enough (batch row, channel) parallelism by itself).
+ */
+size_t ss_scan_fwd_workspace_size(int B, int L, int D, int N, int chunk, int dtype);
+
+/*
  * ss_scan_fwd — selective-scan forward.
  *
  * The diagonal selective SSM trained by backpropagation through time in the
@@ -83,12 +89,19 @@ int ss_scan_num_chunks(int L, int chunk);
  *                 lets the backward skip its recompute pass at the price of
  *                 N*4 bytes of checkpoint per 8 steps and channel.
  *   N           : 4, 8 or 16;  D: a multiple of 8
+ *   workspace   : device scratch of at least ss_scan_fwd_workspace_size()
+ *                 bytes (NULL allowed when that is 0), 16-byte aligned,
+ *                 contents need not be initialised.  When B*D is small the
+ *                 sequence is cut into segments; the scratch holds each
+ *                 segment's zero-start end state and its sum of delta, from
+ *                 which every segment composes the state it starts from.
  * Alignment: every pointer 16-byte aligned.
  */
 int ss_scan_fwd(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm,
                 const float* Dv, const void* z, const float* h0,
                 void* y, float* ckpt, float* h_last,
-                int B, int L, int D, int N, int chunk, int dtype, void* stream);
+                int B, int L, int D, int N, int chunk, int dtype,
+                void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Workspace bytes ss_scan_bwd needs for these sizes (0 on invalid sizes).

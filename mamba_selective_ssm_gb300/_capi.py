@@ -30,7 +30,8 @@ _sz = ctypes.c_size_t
 SIGNATURES = {
     "ss_strerror": (ctypes.c_char_p, [_i]),
     "ss_scan_num_chunks": (_i, [_i, _i]),
-    "ss_scan_fwd": (_i, [_vp] * 11 + [_i] * 6 + [_vp]),
+    "ss_scan_fwd_workspace_size": (_sz, [_i] * 6),
+    "ss_scan_fwd": (_i, [_vp] * 11 + [_i] * 6 + [_vp, _sz, _vp]),
     "ss_scan_bwd_workspace_size": (_sz, [_i] * 6),
     "ss_scan_bwd": (_i, [_vp] * 18 + [_i] * 6 + [_vp, _sz, _vp]),
     "conv1d_causal_bwd_workspace_size": (_sz, [_i] * 4),

@@ -81,10 +81,134 @@ struct BwdParams {
   float* dz;
   float* dh0;
   float* ws_dBC;  // [channel tiles][B][L][2N]
-  float* ws_dAD;  // [gy][D*N + D]: dA then dD partials of each CTA row
+  float* ws_dAD;  // [CTA rows][D*N + D]: dA then dD partials of each CTA row
   int B, L, D, chunk, nchunks;
   uint32_t tcols;
+  int P, Ls;      // sequence segments (P = 1: one CTA row walks whole batch rows)
+  float* gsum;    // [B][P][D][N] adjoint a_tb G_tb at each segment's start from a zero carry at its end
+  float* dsum;    // [B][P][D]    sum of delta over each segment
 };
+
+template <typename T, int N, int NSTG, int DT>
+struct BwdSumSmem {
+  alignas(128) T dlt[NSTG][kTT * DT];
+  alignas(128) T z[NSTG][kTT * DT];
+  alignas(128) T dy[NSTG][kTT * DT];
+  alignas(128) T Cm[NSTG][kTT * N];
+  alignas(16) float dlt_f[kTT * DT];
+  alignas(16) float ds_f[kTT * DT];
+  alignas(16) float C_f[kTT * N];
+  alignas(8) uint64_t full[NSTG];
+};
+
+// Segment summaries for segments 1 .. P-1: the adjoint each carries out of its
+// first step when the carry entering its last step is zero, and its sum of
+// delta.  CTA = (channel tile, (batch row, segment)); tiles walked last to first.
+template <int N, typename T, int NSTG, int DT>
+__global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const BwdParams p,
+                                                                       const __grid_constant__ CUtensorMap tm_dlt,
+                                                                       const __grid_constant__ CUtensorMap tm_z,
+                                                                       const __grid_constant__ CUtensorMap tm_dy,
+                                                                       const __grid_constant__ CUtensorMap tm_C) {
+  using G = Geo<N, DT>;
+  using AT = ActT<T>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  BwdSumSmem<T, N, NSTG, DT>& S = *reinterpret_cast<BwdSumSmem<T, N, NSTG, DT>*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ng = lane % G::NG, cg = lane / G::NG;
+  const int dl = warp * G::WC + cg * 2;
+  const int d0 = blockIdx.x * DT;
+  const int dg = d0 + dl;
+  const bool dvalid = dg < p.D;
+  const int n0 = ng * 4;
+  const int b = (int)blockIdx.y / (p.P - 1), sgm = 1 + (int)blockIdx.y % (p.P - 1);
+  const int tb = sgm * p.Ls, te = min(p.L, tb + p.Ls);
+  const int gtb = tb / kTT, gte = (te + kTT - 1) / kTT;
+  const int nitems = gte - gtb;
+  constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
+  constexpr uint32_t kStageBytes = 3 * kActBytes + kTT * N * AT::kBytes;
+  float2 Ap[2][2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float* a = p.A + (size_t)(dvalid ? dg + j : 0) * N + n0 + 2 * q;
+      Ap[j][q] = dvalid ? f2(a[0] * kLog2e, a[1] * kLog2e) : f2(0.f, 0.f);
+    }
+  auto issue = [&](int k) {
+    const int slot = k % NSTG, t0 = (gte - 1 - k) * kTT;
+    mbar_arrive_expect_tx(&S.full[slot], kStageBytes);
+    tma_load_3d(S.dlt[slot], &tm_dlt, &S.full[slot], d0, t0, b);
+    tma_load_3d(S.z[slot], &tm_z, &S.full[slot], d0, t0, b);
+    tma_load_3d(S.dy[slot], &tm_dy, &S.full[slot], d0, t0, b);
+    tma_load_2d(S.Cm[slot], &tm_C, &S.full[slot], t0 * N, b);
+  };
+  if (tid == 0) {
+    prefetch_tmap(&tm_dlt); prefetch_tmap(&tm_z); prefetch_tmap(&tm_dy); prefetch_tmap(&tm_C);
+    for (int st = 0; st < NSTG; ++st) mbar_init(&S.full[st], 1);
+    fence_barrier_init();
+    for (int k = 0; k < NSTG && k < nitems; ++k) issue(k);
+  }
+  __syncthreads();
+  float2 ga[2][2];
+  float dsum[2] = {0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) ga[j][0] = ga[j][1] = f2(0.f, 0.f);
+  for (int k = 0; k < nitems; ++k) {
+    const int slot = k % NSTG;
+    bool ok = true;
+    if (tid == 0) ok = mbar_wait_bounded(&S.full[slot], (k / NSTG) & 1, kWaitLimitNs);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicOr(&g_bwd_err, kErrTmaTimeout);
+        for (int k2 = k; k2 < k + NSTG && k2 < nitems; ++k2)
+          mbar_wait_bounded(&S.full[k2 % NSTG], (k2 / NSTG) & 1, 100000000ull);
+      }
+      return;
+    }
+    for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
+      float dv[4], zv[4], gv[4];
+      AT::ld4(&S.dlt[slot][gi * 4], dv);
+      AT::ld4(&S.z[slot][gi * 4], zv);
+      AT::ld4(&S.dy[slot][gi * 4], gv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) gv[e] *= zv[e] * sigmoid(zv[e]);
+      reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
+      reinterpret_cast<float4*>(S.ds_f)[gi] = make_float4(gv[0], gv[1], gv[2], gv[3]);
+    }
+    for (int gi = tid; gi < kTT * N / 4; gi += G::NT) {
+      float cv[4];
+      AT::ld4(&S.Cm[slot][gi * 4], cv);
+      reinterpret_cast<float4*>(S.C_f)[gi] = make_float4(cv[0], cv[1], cv[2], cv[3]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = kTT - 1; r >= 0; --r) {
+      const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[r * DT + dl]);
+      const float2 gg = *reinterpret_cast<const float2*>(&S.ds_f[r * DT + dl]);
+      const float4 Cv = *reinterpret_cast<const float4*>(&S.C_f[r * N + n0]);
+      const float2 C01 = f2(Cv.x, Cv.y), C23 = f2(Cv.z, Cv.w);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float dj = j ? dd.y : dd.x;
+        const float2 d2 = bc2(dj), gj = bc2(j ? gg.y : gg.x);
+        dsum[j] += dj;
+        ga[j][0] = mul2(ex2_2(mul2(d2, Ap[j][0])), fma2(gj, C01, ga[j][0]));
+        ga[j][1] = mul2(ex2_2(mul2(d2, Ap[j][1])), fma2(gj, C23, ga[j][1]));
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && k + NSTG < nitems) issue(k + NSTG);
+  }
+  if (dvalid) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const size_t row = ((size_t)b * p.P + sgm) * p.D + dg + j;
+      *reinterpret_cast<float4*>(p.gsum + row * N + n0) = make_float4(ga[j][0].x, ga[j][0].y, ga[j][1].x, ga[j][1].y);
+      if (ng == 0) p.dsum[row] = dsum[j];
+    }
+  }
+}
 
 template <int N, typename T, int NSTG, int DT>
 __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
@@ -106,12 +230,20 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
   const bool dvalid = dg < p.D;
   const int n0 = ng * 4;
   const int L = p.L;
-  const int ntiles = (L + kTT - 1) / kTT;
-  const int tpc = p.chunk / kTT;                        // tiles per full chunk
-  const int ntl = ntiles - (p.nchunks - 1) * tpc;       // tiles in the last chunk
+  // P = 1: CTA row y walks batch rows y, y + gridDim.y, ... whole.
+  // P > 1: CTA row y owns one segment [tb, te) of batch row y / P; segments are
+  // whole chunks and whole tiles, so only the last one can be ragged.
+  const bool segs = p.P > 1;
+  const int sgm = segs ? (int)blockIdx.y % p.P : 0;
+  const int tb = sgm * p.Ls, te = segs ? min(L, tb + p.Ls) : L;
+  const int gtb = tb / kTT, gte = (te + kTT - 1) / kTT;  // tiles [gtb, gte)
+  const int ntiles = gte - gtb;
   const bool direct = p.chunk == kS;                    // a checkpoint per window: no pass A
+  const int tpc = direct ? 1 : p.chunk / kTT;           // tiles per full chunk
+  const int ce = direct ? 0 : (te + p.chunk - 1) / p.chunk;  // chunks [tb / chunk, ce)
+  const int ntl = gte - (ce - 1) * tpc;                 // tiles in the segment's last chunk
   const int per_b = direct ? ntiles : 2 * ntiles;       // items per batch row
-  const int nb = (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
+  const int nb = segs ? 1 : (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
   const int nitems = nb * per_b;
   constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
   constexpr uint32_t kBCBytes = kTT * N * AT::kBytes;
@@ -132,23 +264,23 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
 
   // item k -> (batch row, tile of the sequence, pass; lastA: last pass-A tile of its chunk)
   auto decode = [&](int k, int& b, int& gt, bool& passB, bool& lastA) {
-    b = (int)blockIdx.y + (k / per_b) * (int)gridDim.y;
+    b = segs ? (int)blockIdx.y / p.P : (int)blockIdx.y + (k / per_b) * (int)gridDim.y;
     const int q = k % per_b;
     if (direct) {
-      gt = ntiles - 1 - q;
+      gt = gte - 1 - q;
       passB = true;
       lastA = false;
       return;
     }
     int kc, tl, ntc;
     if (q < 2 * ntl) {
-      kc = p.nchunks - 1;
+      kc = ce - 1;
       ntc = ntl;
       passB = q >= ntl;
       tl = passB ? ntl - 1 - (q - ntl) : q;
     } else {
       const int q2 = q - 2 * ntl;
-      kc = p.nchunks - 2 - q2 / (2 * tpc);
+      kc = ce - 2 - q2 / (2 * tpc);
       ntc = tpc;
       const int r = q2 % (2 * tpc);
       passB = r >= tpc;
@@ -209,7 +341,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
     const int t0 = gt * kTT;
     const int kc = gt / tpc, tl = gt % tpc;
 
-    if (k % per_b == 0) {  // entering batch row b: the gradient arriving on h_{L-1}
+    if (k % per_b == 0) {  // entering batch row b: the gradient arriving on h_{te-1}
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -217,6 +349,17 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
           v = *reinterpret_cast<const float4*>(p.dh_last + ((size_t)b * p.D + dg + j) * N + n0);
         ga[j][0] = f2(v.x, v.y);
         ga[j][1] = f2(v.z, v.w);
+        // carry back through the later segments: ga <- exp2(A' sum(delta)) ga + ga_segment
+        if (segs && dvalid) {
+#pragma unroll 4
+          for (int s2 = p.P - 1; s2 > sgm; --s2) {
+            const size_t row = ((size_t)b * p.P + s2) * p.D + dg + j;
+            const float2 ds2 = bc2(p.dsum[row]);
+            const float4 gs = *reinterpret_cast<const float4*>(p.gsum + row * N + n0);
+            ga[j][0] = fma2(ex2_2(mul2(ds2, Ap[j][0])), ga[j][0], f2(gs.x, gs.y));
+            ga[j][1] = fma2(ex2_2(mul2(ds2, Ap[j][1])), ga[j][1], f2(gs.z, gs.w));
+          }
+        }
       }
     }
 
@@ -557,20 +700,34 @@ struct DADStore {
   }
 };
 
+// Channels per CTA of a launch: with a recompute pass (chunk > 8) the TMEM
+// columns a CTA holds grow with the chunk; from 128 columns (at most four CTAs
+// per SM) a CTA takes 64 channels so that its four warps use all 128 TMEM lanes.
+inline int bwd_channels(int N, int chunk) {
+  const int dt = N == 4 ? bwd_dt<4>() : N == 8 ? bwd_dt<8>() : bwd_dt<16>();
+  return (chunk != kS && tmem_cols(chunk) >= 128u) ? 64 : dt;
+}
+
+inline int bwd_seg_unit(int chunk) { return chunk > kTT ? chunk : kTT; }
+
 struct BwdPlan {
-  int ndt, gy;
-  size_t off_dAD, total;
+  int ndt, gy, pmax;
+  size_t off_dAD, off_gsum, off_dsum, total;
 };
 
-inline BwdPlan make_plan(int B, int L, int D, int N) {
+inline BwdPlan make_plan(int B, int L, int D, int N, int chunk) {
   BwdPlan pl;
-  const int dt = N == 4 ? bwd_dt<4>() : N == 8 ? bwd_dt<8>() : bwd_dt<16>();
-  pl.ndt = (D + dt - 1) / dt;
+  pl.ndt = (D + bwd_channels(N, chunk) - 1) / bwd_channels(N, chunk);
   const int cap = 1024 / pl.ndt > 0 ? 1024 / pl.ndt : 1;
   pl.gy = B < cap ? B : cap;
-  const size_t bc = (size_t)pl.ndt * B * L * 2 * N * sizeof(float);
-  pl.off_dAD = (bc + 255) & ~(size_t)255;
-  pl.total = pl.off_dAD + (size_t)pl.gy * D * (N + 1) * sizeof(float);
+  const long long ctas = (long long)pl.ndt * B;
+  pl.pmax = ctas >= 608 ? 1 : seg_pmax(ctas, L, bwd_seg_unit(chunk));
+  const int rows = pl.pmax > 1 && B * pl.pmax > pl.gy ? B * pl.pmax : pl.gy;
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  pl.off_dAD = up((size_t)pl.ndt * B * L * 2 * N * sizeof(float));
+  pl.off_gsum = up(pl.off_dAD + (size_t)rows * D * (N + 1) * sizeof(float));
+  pl.off_dsum = up(pl.off_gsum + (pl.pmax > 1 ? (size_t)B * pl.pmax * D * N * sizeof(float) : 0));
+  pl.total = pl.off_dsum + (pl.pmax > 1 ? (size_t)B * pl.pmax * D * sizeof(float) : 0);
   return pl;
 }
 
@@ -584,9 +741,11 @@ template <int N, typename T, int NSTG = Stages<T>::value, int DT = bwd_dt<N>()>
 int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, const void* dy,
                float* dA, float* dB, float* dC, float* dD, void* ws, cudaStream_t stream) {
   constexpr int e = ActT<T>::kBytes;
-  const BwdPlan pl = make_plan(p.B, p.L, p.D, N);
+  const BwdPlan pl = make_plan(p.B, p.L, p.D, N, p.chunk);
   p.ws_dBC = static_cast<float*>(ws);
   p.ws_dAD = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_dAD);
+  p.gsum = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_gsum);
+  p.dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_dsum);
   p.tcols = p.chunk == kS ? 0u : tmem_cols(p.chunk);
   CUtensorMap tm[6];
   const uint64_t adims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
@@ -622,7 +781,28 @@ int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, co
       return SS_ERR_CUDA;
     if ((uint32_t)per_sm * p.tcols > 512u) return SS_ERR_UNSUPPORTED;
   }
-  kern<<<dim3(pl.ndt, pl.gy), Geo<N, DT>::NT, smem_launch, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4], tm[5]);
+  // segments: only when (batch row, channel tile) pairs leave resident CTA slots idle
+  p.P = 1;
+  p.Ls = p.L;
+  if (pl.pmax > 1) {
+    const long long resident = (long long)per_sm * device_sm_count();
+    int want = (int)(resident / ((long long)pl.ndt * p.B));
+    if (want > pl.pmax) want = pl.pmax;
+    const SegPlan sp = seg_plan(want, p.L, bwd_seg_unit(p.chunk));
+    p.P = sp.P;
+    p.Ls = sp.Ls;
+  }
+  int rows = pl.gy;
+  if (p.P > 1) {
+    rows = p.B * p.P;
+    const size_t smem_s = sizeof(BwdSumSmem<T, N, NSTG, DT>);
+    auto skern = scan_bwd_summary_kernel<N, T, NSTG, DT>;
+    if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s) != cudaSuccess)
+      return SS_ERR_CUDA;
+    skern<<<dim3(pl.ndt, p.B * (p.P - 1)), Geo<N, DT>::NT, smem_s, stream>>>(p, tm[0], tm[2], tm[3], tm[5]);
+    if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+  }
+  kern<<<dim3(pl.ndt, rows), Geo<N, DT>::NT, smem_launch, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4], tm[5]);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
   const long long nBC = (long long)p.B * p.L * 2 * N;
   long long blocks = (nBC + 255) / 256;
@@ -630,7 +810,7 @@ int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, co
   ss_bwd_dbc_kernel<N><<<(int)blocks, 256, 0, stream>>>(p.ws_dBC, dB, dC, nBC, pl.ndt);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
   const long long nA = (long long)p.D * N;
-  return colsum(p.ws_dAD, nA + p.D, pl.gy, DADStore{dA, dD, nA}, stream) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  return colsum(p.ws_dAD, nA + p.D, rows, DADStore{dA, dD, nA}, stream) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 int validate_bwd(int B, int L, int D, int N, int chunk, int dtype) {
@@ -657,7 +837,7 @@ int read_clear_bwd_err(cudaStream_t s, unsigned* out) {
 
 extern "C" size_t ss_scan_bwd_workspace_size(int B, int L, int D, int N, int chunk, int dtype) {
   if (validate_bwd(B, L, D, N, chunk, dtype) != SS_OK) return 0;
-  return make_plan(B, L, D, N).total;
+  return make_plan(B, L, D, N, chunk).total;
 }
 
 extern "C" int ss_scan_bwd(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm, const float* Dv,
@@ -672,17 +852,25 @@ extern "C" int ss_scan_bwd(const void* x, const void* delta, const float* A, con
   for (const void* q : ptrs)
     if (!ssh::aligned16(q)) return SS_ERR_ALIGN;
   if ((dh_last && !ssh::aligned16(dh_last)) || (dh0 && !ssh::aligned16(dh0))) return SS_ERR_ALIGN;
-  const BwdPlan pl = make_plan(B, L, D, N);
+  const BwdPlan pl = make_plan(B, L, D, N, chunk);
   if (workspace == nullptr || ws_bytes < pl.total) return SS_ERR_WORKSPACE;
   if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
-  BwdParams p{A, Dv, ckpt, dh_last, dx, ddelta, dz, dh0, nullptr, nullptr, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 0};
+  BwdParams p{A, Dv, ckpt, dh_last, dx, ddelta, dz, dh0, nullptr, nullptr, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 0,
+              1, L, nullptr, nullptr};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool wide = bwd_channels(N, chunk) == 64;
   if (dtype == SS_F32) {
     if (N == 4) return launch_bwd<4, float>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
-    if (N == 8) return launch_bwd<8, float>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
-    return launch_bwd<16, float>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
+    if (N == 8)
+      return wide ? launch_bwd<8, float, Stages<float>::value, 64>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s)
+                  : launch_bwd<8, float>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
+    return wide ? launch_bwd<16, float, Stages<float>::value, 64>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s)
+                : launch_bwd<16, float>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
   }
   if (N == 4) return launch_bwd<4, __nv_bfloat16>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
-  if (N == 8) return launch_bwd<8, __nv_bfloat16>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
-  return launch_bwd<16, __nv_bfloat16>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
+  if (N == 8)
+    return wide ? launch_bwd<8, __nv_bfloat16, Stages<__nv_bfloat16>::value, 64>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s)
+                : launch_bwd<8, __nv_bfloat16>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
+  return wide ? launch_bwd<16, __nv_bfloat16, Stages<__nv_bfloat16>::value, 64>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s)
+              : launch_bwd<16, __nv_bfloat16>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
 }

@@ -31,4 +31,40 @@ struct Geo {
   static_assert(W >= 1 && DT % WC == 0, "a CTA holds whole warps");
 };
 
+// ---------------------------------------------------------------- sequence segments
+// When a layer has too few (batch, channel-tile) pairs to fill the GPU, the
+// sequence is cut into P segments of Ls steps (a multiple of `unit`).  A
+// summary kernel computes each segment's contribution from a zero carry and
+// its total step size sum(delta); a main-kernel CTA then composes its own
+// carry from the summaries of the segments before (forward) or after
+// (backward) it:  carry <- exp2(A log2e * sum(delta)) * carry + contribution.
+
+// Upper bound on P used to size the summary workspace: aims at ~2400 CTAs.
+inline int seg_pmax(long long ctas, int L, int unit) {
+  long long pm = (2432 + ctas - 1) / ctas;
+  const long long units = (L + unit - 1) / unit;
+  if (pm > 64) pm = 64;
+  if (pm > units) pm = units;
+  return pm < 1 ? 1 : (int)pm;
+}
+
+struct SegPlan {
+  int P, Ls;
+};
+
+// Segments of equal length (a multiple of unit) covering L with about p_want pieces.
+inline SegPlan seg_plan(int p_want, int L, int unit) {
+  if (p_want <= 1) return SegPlan{1, L};
+  const int per = (L + p_want - 1) / p_want;
+  const int Ls = ((per + unit - 1) / unit) * unit;
+  return SegPlan{(L + Ls - 1) / Ls, Ls};
+}
+
+inline int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
 }  // namespace ssk

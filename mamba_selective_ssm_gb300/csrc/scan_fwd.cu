@@ -63,7 +63,124 @@ struct FwdParams {
   float* ckpt;
   float* h_last;
   int B, L, D, chunk, nchunks;
+  int P, Ls;     // sequence segments (P = 1: one CTA row walks whole batch rows)
+  float* hsum;   // [B][P][D][N] state at the end of each segment from a zero start
+  float* dsum;   // [B][P][D]    sum of delta over each segment
 };
+
+template <typename T, int N, int DT>
+struct FwdSumSmem {
+  alignas(128) T dlt[kNST][kTT * DT];
+  alignas(128) T x[kNST][kTT * DT];
+  alignas(128) T Bm[kNST][kTT * N];
+  alignas(16) float dlt_f[kTT * DT];
+  alignas(16) float dx_f[kTT * DT];
+  alignas(16) float B_f[kTT * N];
+  alignas(8) uint64_t full[kNST];
+};
+
+// Segment summaries for segments 0 .. P-2: the state each reaches from a zero
+// start, and its sum of delta.  CTA = (channel tile, (batch row, segment)).
+template <int N, typename T, int CPT, int DT>
+__global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_summary_kernel(const FwdParams p,
+                                                                      const __grid_constant__ CUtensorMap tm_dlt,
+                                                                      const __grid_constant__ CUtensorMap tm_x,
+                                                                      const __grid_constant__ CUtensorMap tm_B) {
+  using G = GeoF<N, CPT, DT>;
+  using AT = ActT<T>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  FwdSumSmem<T, N, DT>& S = *reinterpret_cast<FwdSumSmem<T, N, DT>*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ng = lane % G::NG, cg = lane / G::NG;
+  const int dl = warp * G::WC + cg * CPT;
+  const int d0 = blockIdx.x * DT;
+  const int dg = d0 + dl;
+  const bool dvalid = dg < p.D;
+  const int n0 = ng * 4;
+  const int b = (int)blockIdx.y / (p.P - 1), sgm = (int)blockIdx.y % (p.P - 1);
+  const int tb = sgm * p.Ls;
+  const int nitems = p.Ls / kTT;  // segments before the last are whole
+  constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
+  constexpr uint32_t kStageBytes = 2 * kActBytes + kTT * N * AT::kBytes;
+  float2 Ap[CPT][2];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float* a = p.A + (size_t)(dvalid ? dg + j : 0) * N + n0 + 2 * q;
+      Ap[j][q] = dvalid ? f2(a[0] * kLog2e, a[1] * kLog2e) : f2(0.f, 0.f);
+    }
+  auto issue = [&](int k) {
+    const int slot = k % kNST, t0 = tb + k * kTT;
+    mbar_arrive_expect_tx(&S.full[slot], kStageBytes);
+    tma_load_3d(S.dlt[slot], &tm_dlt, &S.full[slot], d0, t0, b);
+    tma_load_3d(S.x[slot], &tm_x, &S.full[slot], d0, t0, b);
+    tma_load_2d(S.Bm[slot], &tm_B, &S.full[slot], t0 * N, b);
+  };
+  if (tid == 0) {
+    prefetch_tmap(&tm_dlt); prefetch_tmap(&tm_x); prefetch_tmap(&tm_B);
+    for (int st = 0; st < kNST; ++st) mbar_init(&S.full[st], 1);
+    fence_barrier_init();
+    for (int k = 0; k < kNST && k < nitems; ++k) issue(k);
+  }
+  __syncthreads();
+  float2 h[CPT][2];
+  float dsum[CPT];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    h[j][0] = h[j][1] = f2(0.f, 0.f);
+    dsum[j] = 0.f;
+  }
+  for (int k = 0; k < nitems; ++k) {
+    const int slot = k % kNST;
+    bool ok = true;
+    if (tid == 0) ok = mbar_wait_bounded(&S.full[slot], (k / kNST) & 1, kWaitLimitNs);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicOr(&g_fwd_err, kErrTmaTimeout);
+        for (int k2 = k; k2 < k + kNST && k2 < nitems; ++k2)
+          mbar_wait_bounded(&S.full[k2 % kNST], (k2 / kNST) & 1, 100000000ull);
+      }
+      return;
+    }
+    for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
+      float dv[4], xv[4];
+      AT::ld4(&S.dlt[slot][gi * 4], dv);
+      AT::ld4(&S.x[slot][gi * 4], xv);
+      reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
+      reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(dv[0] * xv[0], dv[1] * xv[1], dv[2] * xv[2], dv[3] * xv[3]);
+    }
+    for (int gi = tid; gi < kTT * N / 4; gi += G::NT) {
+      float bv[4];
+      AT::ld4(&S.Bm[slot][gi * 4], bv);
+      reinterpret_cast<float4*>(S.B_f)[gi] = make_float4(bv[0], bv[1], bv[2], bv[3]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kTT; ++r) {
+      const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
+      const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) {
+        const float dd = S.dlt_f[r * DT + dl + j];
+        const float2 dj = bc2(dd), xj = bc2(S.dx_f[r * DT + dl + j]);
+        dsum[j] += dd;
+        h[j][0] = fma2(ex2_2(mul2(dj, Ap[j][0])), h[j][0], mul2(xj, B01));
+        h[j][1] = fma2(ex2_2(mul2(dj, Ap[j][1])), h[j][1], mul2(xj, B23));
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && k + kNST < nitems) issue(k + kNST);
+  }
+  if (dvalid) {
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      const size_t row = ((size_t)b * p.P + sgm) * p.D + dg + j;
+      *reinterpret_cast<float4*>(p.hsum + row * N + n0) = make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
+      if (ng == 0) p.dsum[row] = dsum[j];
+    }
+  }
+}
 
 template <int N, typename T, int CPT, int DT>
 __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
@@ -84,9 +201,16 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
   const bool dvalid = dg < p.D;  // D is a multiple of 8, so dg+CPT-1 < D as well
   const int n0 = ng * 4;
   const int L = p.L;
-  const int ntiles = (L + kTT - 1) / kTT;
-  const int nb = (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;  // batch rows of this CTA
+  // P = 1: CTA row y walks batch rows y, y + gridDim.y, ... whole.
+  // P > 1: CTA row y owns one segment [tb, te) of batch row y / P.
+  const bool segs = p.P > 1;
+  const int sgm = segs ? (int)blockIdx.y % p.P : 0;
+  const int tb = sgm * p.Ls;
+  const int te = segs ? min(L, tb + p.Ls) : L;
+  const int ntiles = (te - tb + kTT - 1) / kTT;
+  const int nb = segs ? 1 : (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;  // batch rows of this CTA
   const int nitems = nb * ntiles;
+  auto row_of = [&](int k) { return segs ? (int)blockIdx.y / p.P : (int)blockIdx.y + (k / ntiles) * (int)gridDim.y; };
   constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
   constexpr uint32_t kBCBytes = kTT * N * AT::kBytes;
   constexpr uint32_t kStageBytes = 3 * kActBytes + 2 * kBCBytes;
@@ -108,8 +232,8 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
 
   auto issue = [&](int k) {
     const int slot = k % kNST;
-    const int bb = (int)blockIdx.y + (k / ntiles) * (int)gridDim.y;
-    const int t0 = (k % ntiles) * kTT;
+    const int bb = row_of(k);
+    const int t0 = tb + (k % ntiles) * kTT;
     mbar_arrive_expect_tx(&S.full[slot], kStageBytes);
     tma_load_3d(S.dlt[slot], &tm_dlt, &S.full[slot], d0, t0, bb);
     tma_load_3d(S.x[slot], &tm_x, &S.full[slot], d0, t0, bb);
@@ -129,9 +253,9 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
   float2 h[CPT][2];
   for (int k = 0; k < nitems; ++k) {
     const int slot = k % kNST;
-    const int b = (int)blockIdx.y + (k / ntiles) * (int)gridDim.y;
+    const int b = row_of(k);
     const int ti = k % ntiles;
-    const int t0 = ti * kTT;
+    const int t0 = tb + ti * kTT;
 
     if (ti == 0) {  // entering batch row b: initial state
 #pragma unroll
@@ -140,6 +264,17 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
         if (p.h0 != nullptr && dvalid) v = *reinterpret_cast<const float4*>(p.h0 + ((size_t)b * p.D + dg + j) * N + n0);
         h[j][0] = f2(v.x, v.y);
         h[j][1] = f2(v.z, v.w);
+        // carry through the earlier segments: h <- exp2(A' sum(delta)) h + h_segment
+        if (dvalid) {
+#pragma unroll 4
+          for (int s2 = 0; s2 < sgm; ++s2) {
+            const size_t row = ((size_t)b * p.P + s2) * p.D + dg + j;
+            const float2 ds2 = bc2(p.dsum[row]);
+            const float4 hs = *reinterpret_cast<const float4*>(p.hsum + row * N + n0);
+            h[j][0] = fma2(ex2_2(mul2(ds2, Ap[j][0])), h[j][0], f2(hs.x, hs.y));
+            h[j][1] = fma2(ex2_2(mul2(ds2, Ap[j][1])), h[j][1], f2(hs.z, hs.w));
+          }
+        }
       }
     }
 
@@ -249,7 +384,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
     __syncthreads();
     if (tid == 0 && k + kNST < nitems) issue(k + kNST);
 
-    if (ti == ntiles - 1 && p.h_last != nullptr && dvalid) {
+    if (ti == ntiles - 1 && te == L && p.h_last != nullptr && dvalid) {
 #pragma unroll
       for (int j = 0; j < CPT; ++j)
         *reinterpret_cast<float4*>(p.h_last + ((size_t)b * p.D + dg + j) * N + n0) =
@@ -258,8 +393,20 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
   }
 }
 
+template <int N>
+int fwd_pmax(int B, int L, int D) {
+  const long long ctas = (long long)((D + kFDT - 1) / kFDT) * B;
+  return ctas >= 608 ? 1 : seg_pmax(ctas, L, kTT);
+}
+
+size_t fwd_ws_bytes(int B, int L, int D, int N) {
+  const int pm = N == 4 ? fwd_pmax<4>(B, L, D) : N == 8 ? fwd_pmax<8>(B, L, D) : fwd_pmax<16>(B, L, D);
+  if (pm <= 1) return 0;
+  return (((size_t)B * pm * D * N * sizeof(float) + 255) & ~(size_t)255) + (size_t)B * pm * D * sizeof(float);
+}
+
 template <int N, typename T, int CPT = 1, int DT = kFDT>
-int launch_fwd(const FwdParams& p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z,
+int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, void* ws,
                cudaStream_t stream) {
   constexpr int e = ActT<T>::kBytes;
   CUtensorMap tm[5];
@@ -276,12 +423,39 @@ int launch_fwd(const FwdParams& p, const void* x, const void* delta, const void*
       !ssh::encode_tiled(&tm[4], ActT<T>::kTma, 2, Cm, bdims, bstr, bbox))
     return SS_ERR_CUDA;
   const int ndt = (p.D + DT - 1) / DT;
-  const int cap = 1024 / ndt > 0 ? 1024 / ndt : 1;  // about 1024 CTAs; each loops over its batch rows
-  const int gy = p.B < cap ? p.B : cap;
   const size_t smem = sizeof(FwdSmem<T, N, DT>);
   auto kern = scan_fwd_kernel<N, T, CPT, DT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
-  kern<<<dim3(ndt, gy), GeoF<N, CPT, DT>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
+  // segments: only when (batch row, channel tile) pairs leave SMs idle
+  p.P = 1;
+  p.Ls = p.L;
+  const int pmax = fwd_pmax<N>(p.B, p.L, p.D);
+  if (pmax > 1) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, GeoF<N, CPT, DT>::NT, smem) != cudaSuccess)
+      return SS_ERR_CUDA;
+    const long long resident = (long long)per_sm * device_sm_count();
+    int want = (int)(resident / ((long long)ndt * p.B));
+    if (want > pmax) want = pmax;
+    const SegPlan sp = seg_plan(want, p.L, kTT);
+    p.P = sp.P;
+    p.Ls = sp.Ls;
+    p.hsum = static_cast<float*>(ws);
+    p.dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + (((size_t)p.B * pmax * p.D * N * sizeof(float) + 255) & ~(size_t)255));
+  }
+  if (p.P > 1) {
+    const size_t smem_s = sizeof(FwdSumSmem<T, N, DT>);
+    auto skern = scan_fwd_summary_kernel<N, T, CPT, DT>;
+    if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s) != cudaSuccess)
+      return SS_ERR_CUDA;
+    skern<<<dim3(ndt, p.B * (p.P - 1)), GeoF<N, CPT, DT>::NT, smem_s, stream>>>(p, tm[0], tm[1], tm[3]);
+    if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+    kern<<<dim3(ndt, p.B * p.P), GeoF<N, CPT, DT>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
+  } else {
+    const int cap = 1024 / ndt > 0 ? 1024 / ndt : 1;  // about 1024 CTAs; each loops over its batch rows
+    const int gy = p.B < cap ? p.B : cap;
+    kern<<<dim3(ndt, gy), GeoF<N, CPT, DT>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
+  }
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
@@ -298,10 +472,8 @@ int read_clear_fwd_err(cudaStream_t s, unsigned* out) {
 
 extern "C" int ss_scan_num_chunks(int L, int chunk) { return (L > 0 && chunk > 0) ? (L + chunk - 1) / chunk : 0; }
 
-extern "C" int ss_scan_fwd(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm, const float* Dv,
-                           const void* z, const float* h0, void* y, float* ckpt, float* h_last, int B, int L, int D, int N,
-                           int chunk, int dtype, void* stream) {
-  if (!x || !delta || !A || !Bm || !Cm || !Dv || !z || !y || !ckpt) return SS_ERR_NULL;
+namespace {
+int validate_fwd(int B, int L, int D, int N, int chunk, int dtype) {
   if (B <= 0 || L <= 0 || D <= 0 || N <= 0 || chunk <= 0) return SS_ERR_DIM;
   if (N != 4 && N != 8 && N != 16) return SS_ERR_UNSUPPORTED;
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
@@ -309,20 +481,39 @@ extern "C" int ss_scan_fwd(const void* x, const void* delta, const float* A, con
   if (D % 8 != 0) return SS_ERR_ALIGN;
   // the B_t / C_t rows of one batch element must span a multiple of 16 bytes (TMA stride rule)
   if (((long long)L * N * (dtype == SS_F32 ? 4 : 2)) % 16 != 0) return SS_ERR_ALIGN;
+  // TMA coordinates and tensor extents are 32-bit
+  if ((long long)L * N >= (1ll << 31) || (long long)L * D >= (1ll << 40)) return SS_ERR_DIM;
+  return SS_OK;
+}
+
+}  // namespace
+
+extern "C" size_t ss_scan_fwd_workspace_size(int B, int L, int D, int N, int chunk, int dtype) {
+  if (validate_fwd(B, L, D, N, chunk, dtype) != SS_OK) return 0;
+  return fwd_ws_bytes(B, L, D, N);
+}
+
+extern "C" int ss_scan_fwd(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm, const float* Dv,
+                           const void* z, const float* h0, void* y, float* ckpt, float* h_last, int B, int L, int D, int N,
+                           int chunk, int dtype, void* workspace, size_t ws_bytes, void* stream) {
+  if (!x || !delta || !A || !Bm || !Cm || !Dv || !z || !y || !ckpt) return SS_ERR_NULL;
+  const int v = validate_fwd(B, L, D, N, chunk, dtype);
+  if (v != SS_OK) return v;
   const void* ptrs[] = {x, delta, A, Bm, Cm, Dv, z, y, ckpt};
   for (const void* q : ptrs)
     if (!ssh::aligned16(q)) return SS_ERR_ALIGN;
   if ((h0 && !ssh::aligned16(h0)) || (h_last && !ssh::aligned16(h_last))) return SS_ERR_ALIGN;
-  // TMA coordinates and tensor extents are 32-bit
-  if ((long long)L * N >= (1ll << 31) || (long long)L * D >= (1ll << 40)) return SS_ERR_DIM;
-  FwdParams p{A, Dv, h0, y, ckpt, h_last, B, L, D, chunk, ss_scan_num_chunks(L, chunk)};
+  const size_t need = fwd_ws_bytes(B, L, D, N);
+  if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SS_ERR_WORKSPACE;
+  if (workspace != nullptr && !ssh::aligned16(workspace)) return SS_ERR_ALIGN;
+  FwdParams p{A, Dv, h0, y, ckpt, h_last, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 1, L, nullptr, nullptr};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SS_F32) {
-    if (N == 4) return launch_fwd<4, float>(p, x, delta, Bm, Cm, z, s);
-    if (N == 8) return launch_fwd<8, float>(p, x, delta, Bm, Cm, z, s);
-    return launch_fwd<16, float>(p, x, delta, Bm, Cm, z, s);
+    if (N == 4) return launch_fwd<4, float>(p, x, delta, Bm, Cm, z, workspace, s);
+    if (N == 8) return launch_fwd<8, float>(p, x, delta, Bm, Cm, z, workspace, s);
+    return launch_fwd<16, float>(p, x, delta, Bm, Cm, z, workspace, s);
   }
-  if (N == 4) return launch_fwd<4, __nv_bfloat16>(p, x, delta, Bm, Cm, z, s);
-  if (N == 8) return launch_fwd<8, __nv_bfloat16>(p, x, delta, Bm, Cm, z, s);
-  return launch_fwd<16, __nv_bfloat16>(p, x, delta, Bm, Cm, z, s);
+  if (N == 4) return launch_fwd<4, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
+  if (N == 8) return launch_fwd<8, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
+  return launch_fwd<16, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
 }

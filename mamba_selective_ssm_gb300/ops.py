@@ -3,7 +3,7 @@ C-ABI call on the current CUDA stream.  No arithmetic of the method is done here
 
 Names and argument order follow include/ssscan.h:
 
-* ``ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk=64)``
+* ``ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk=64, workspace=None)``
   -> ``(y, ckpt, h_last)``
 * ``ss_scan_bwd(x, delta, A, Bm, Cm, Dv, z, ckpt, dy, dh_last=None, chunk=64, dA=None, dD=None, ...)``
   -> dict of gradients
@@ -60,7 +60,11 @@ def num_chunks(L: int, chunk: int) -> int:
     return load().ss_scan_num_chunks(L, chunk)
 
 
-def ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int = 64, want_h_last: bool = True):
+def scan_fwd_workspace_size(B, L, D, N, chunk, dtype) -> int:
+    return load().ss_scan_fwd_workspace_size(B, L, D, N, chunk, _DT[dtype])
+
+
+def ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int = 64, want_h_last: bool = True, workspace=None):
     lib = load()
     B, L, D = x.shape
     N = A.shape[1]
@@ -78,8 +82,12 @@ def ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int = 64, want_h_las
     y = torch.empty_like(x)
     ckpt = torch.empty((B, max(nck, 1), D, N), device=dev, dtype=torch.float32)
     h_last = torch.empty((B, D, N), device=dev, dtype=torch.float32) if want_h_last else None
+    ws_bytes = lib.ss_scan_fwd_workspace_size(B, L, D, N, chunk, _DT[dt])
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    ws_have = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.ss_scan_fwd(_p(x), _p(delta), _p(A), _p(Bm), _p(Cm), _p(Dv), _p(z), _p(h0), _p(y), _p(ckpt), _p(h_last),
-                         B, L, D, N, chunk, _DT[dt], _stream())
+                         B, L, D, N, chunk, _DT[dt], _p(workspace), ws_have, _stream())
     check(rc, "ss_scan_fwd")
     return y, ckpt, h_last
 

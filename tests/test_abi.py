@@ -57,7 +57,7 @@ def test_scan_fwd_validation(lib):
     p = [_fake(0x10000 + 256 * i) for i in range(11)]
 
     def call(ptrs=p, B=2, L=64, D=16, N=4, chunk=64, dtype=c.SS_F32):
-        return lib.ss_scan_fwd(*ptrs, B, L, D, N, chunk, dtype, None)
+        return lib.ss_scan_fwd(*ptrs, B, L, D, N, chunk, dtype, None, 0, None)
 
     q = list(p)
     q[0] = None
@@ -77,6 +77,21 @@ def test_scan_fwd_validation(lib):
     q = list(p)
     q[3] = _fake(0x10004)
     assert call(q) == c.SS_ERR_ALIGN
+
+
+def test_scan_fwd_workspace(lib):
+    """A small B*D cuts the sequence into segments, whose summaries need scratch;
+    a layer with enough (batch row, channel) pairs needs none."""
+    from mamba_selective_ssm_gb300 import _capi as c
+    ws = lib.ss_scan_fwd_workspace_size(2, 64, 16, 4, 64, c.SS_F32)
+    # end states [B, P, D, N] and sums of delta [B, P, D] for P = 64 / 16 segments
+    assert ws >= 2 * 4 * 16 * 4 * 4 + 2 * 4 * 16 * 4
+    assert lib.ss_scan_fwd_workspace_size(8, 2048, 4096, 16, 8, c.SS_BF16) == 0
+    assert lib.ss_scan_fwd_workspace_size(2, 64, 16, 5, 64, c.SS_F32) == 0  # invalid N
+    p = [_fake(0x10000 + 256 * i) for i in range(11)]
+    assert lib.ss_scan_fwd(*p, 2, 64, 16, 4, 64, c.SS_F32, None, 0, None) == c.SS_ERR_WORKSPACE
+    assert lib.ss_scan_fwd(*p, 2, 64, 16, 4, 64, c.SS_F32, _fake(0x90000), ws - 1, None) == c.SS_ERR_WORKSPACE
+    assert lib.ss_scan_fwd(*p, 2, 64, 16, 4, 64, c.SS_F32, _fake(0x90008), ws, None) == c.SS_ERR_ALIGN
 
 
 def test_scan_bwd_validation_and_workspace(lib):

@@ -37,6 +37,11 @@ CASES = [
     (3, 77, 64, 8, "bf16", 8),
     (1, 300, 136, 16, "bf16", 8),
     (2, 5, 8, 4, "f32", 8),
+    # few (batch row, channel tile) pairs: the sequence is cut into segments whose
+    # carries are composed from per-segment summaries; ragged last segments
+    (1, 1000, 64, 16, "bf16", 8),
+    (1, 700, 200, 16, "bf16", 128),  # 64-channel backward CTAs (recompute pass, chunk >= 128)
+    (2, 600, 72, 8, "f32", 256),
 ]
 
 
