@@ -262,37 +262,59 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
     }
   for (int c = tid; c < DT; c += G::NT) S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
 
-  // item k -> (batch row, tile of the sequence, pass; lastA: last pass-A tile of its chunk)
-  auto decode = [&](int k, int& b, int& gt, bool& passB, bool& lastA) {
-    b = segs ? (int)blockIdx.y / p.P : (int)blockIdx.y + (k / per_b) * (int)gridDim.y;
-    const int q = k % per_b;
+  // Items of a batch row, in order.  Direct mode: tiles gte-1 down to gtb.
+  // Otherwise per chunk kc = ce-1 down to tb/chunk: pass A over its ntc tiles
+  // in order, then pass B over them in reverse.  Two cursors (consumer, TMA
+  // issuer) step through the items without divisions.
+  const int kc_first = tb / p.chunk;
+  struct Cursor {
+    int b, kc, tl, ntc;
+    bool passB, first;
+  };
+  auto start_row = [&](Cursor& c, int b) {
+    c.b = b;
+    c.first = true;
     if (direct) {
-      gt = gte - 1 - q;
-      passB = true;
-      lastA = false;
+      c.kc = gte - 1;  // the tile
+      c.tl = 0;
+      c.ntc = 1;
+      c.passB = true;
+    } else {
+      c.kc = ce - 1;
+      c.ntc = ntl;
+      c.tl = 0;
+      c.passB = false;
+    }
+  };
+  auto advance = [&](Cursor& c) {
+    c.first = false;
+    if (direct) {
+      if (--c.kc < gtb) start_row(c, c.b + (int)gridDim.y);
       return;
     }
-    int kc, tl, ntc;
-    if (q < 2 * ntl) {
-      kc = ce - 1;
-      ntc = ntl;
-      passB = q >= ntl;
-      tl = passB ? ntl - 1 - (q - ntl) : q;
-    } else {
-      const int q2 = q - 2 * ntl;
-      kc = ce - 2 - q2 / (2 * tpc);
-      ntc = tpc;
-      const int r = q2 % (2 * tpc);
-      passB = r >= tpc;
-      tl = passB ? tpc - 1 - (r - tpc) : r;
+    if (!c.passB) {
+      if (++c.tl == c.ntc) {
+        c.passB = true;
+        c.tl = c.ntc - 1;
+      }
+    } else if (c.tl-- == 0) {
+      if (--c.kc < kc_first) {
+        start_row(c, c.b + (int)gridDim.y);
+      } else {
+        c.ntc = tpc;
+        c.tl = 0;
+        c.passB = false;
+      }
     }
-    gt = kc * tpc + tl;
-    lastA = !passB && tl == ntc - 1;
   };
-  auto issue = [&](int k) {
-    int b, gt;
-    bool passB, lastA;
-    decode(k, b, gt, passB, lastA);
+  auto tile_of = [&](const Cursor& c) { return direct ? c.kc : c.kc * tpc + c.tl; };
+  const int b_first = segs ? (int)blockIdx.y / p.P : (int)blockIdx.y;
+  Cursor icur;
+  start_row(icur, b_first);
+  auto issue = [&](int k) {  // k: the item icur points at
+    const int b = icur.b, gt = tile_of(icur);
+    const bool passB = icur.passB;
+    advance(icur);
     const int slot = k % NSTG;
     const int t0 = gt * kTT;
     mbar_arrive_expect_tx(&S.full[slot], passB ? 4 * kActBytes + 2 * kBCBytes : 2 * kActBytes + kBCBytes);
@@ -333,15 +355,18 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
   for (int e = 0; e < 4; ++e) dDacc[e] = 0.f;
   bool failed = false;
 
-  for (int k = 0; k < nitems; ++k) {
+  Cursor cur;
+  start_row(cur, b_first);
+  for (int k = 0; k < nitems; ++k, advance(cur)) {
     const int slot = k % NSTG;
-    int b, gt;
-    bool passB, lastA;
-    decode(k, b, gt, passB, lastA);
+    const int b = cur.b;
+    const int gt = tile_of(cur);
+    const bool passB = cur.passB;
+    const bool lastA = !cur.passB && cur.tl == cur.ntc - 1;  // last pass-A tile of its chunk
     const int t0 = gt * kTT;
-    const int kc = gt / tpc, tl = gt % tpc;
+    const int kc = cur.kc, tl = cur.tl;
 
-    if (k % per_b == 0) {  // entering batch row b: the gradient arriving on h_{te-1}
+    if (cur.first) {  // entering batch row b: the gradient arriving on h_{te-1}
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);

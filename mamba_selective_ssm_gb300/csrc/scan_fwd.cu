@@ -210,7 +210,19 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
   const int ntiles = (te - tb + kTT - 1) / kTT;
   const int nb = segs ? 1 : (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;  // batch rows of this CTA
   const int nitems = nb * ntiles;
-  auto row_of = [&](int k) { return segs ? (int)blockIdx.y / p.P : (int)blockIdx.y + (k / ntiles) * (int)gridDim.y; };
+  const int b_first = segs ? (int)blockIdx.y / p.P : (int)blockIdx.y;
+  // items (batch row, tile) in order; two cursors (consumer, TMA issuer) step
+  // through them without divisions
+  struct Cursor {
+    int b, ti;
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.ti == ntiles) {
+      c.ti = 0;
+      c.b += (int)gridDim.y;
+    }
+  };
+  Cursor icur{b_first, 0};
   constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
   constexpr uint32_t kBCBytes = kTT * N * AT::kBytes;
   constexpr uint32_t kStageBytes = 3 * kActBytes + 2 * kBCBytes;
@@ -230,10 +242,11 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
     }
   for (int c = tid; c < DT; c += G::NT) S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
 
-  auto issue = [&](int k) {
+  auto issue = [&](int k) {  // k: the item icur points at
     const int slot = k % kNST;
-    const int bb = row_of(k);
-    const int t0 = tb + (k % ntiles) * kTT;
+    const int bb = icur.b;
+    const int t0 = tb + icur.ti * kTT;
+    advance(icur);
     mbar_arrive_expect_tx(&S.full[slot], kStageBytes);
     tma_load_3d(S.dlt[slot], &tm_dlt, &S.full[slot], d0, t0, bb);
     tma_load_3d(S.x[slot], &tm_x, &S.full[slot], d0, t0, bb);
@@ -251,11 +264,14 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
   __syncthreads();
 
   float2 h[CPT][2];
-  for (int k = 0; k < nitems; ++k) {
+  Cursor cur{b_first, 0};
+  int tck = 0;  // t0 mod chunk (chunk > 8)
+  for (int k = 0; k < nitems; ++k, advance(cur)) {
     const int slot = k % kNST;
-    const int b = row_of(k);
-    const int ti = k % ntiles;
+    const int b = cur.b;
+    const int ti = cur.ti;
     const int t0 = tb + ti * kTT;
+    if (ti == 0) tck = tb % p.chunk;
 
     if (ti == 0) {  // entering batch row b: initial state
 #pragma unroll
@@ -313,8 +329,8 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
       constexpr int kH = kTT / 2;
       // checkpoint: the state entering step t0 + 8 half (chunk is 8 or a multiple of the tile)
       const int tc = t0 + half * kH;
-      if (dvalid && tc < L && (tc % p.chunk) == 0) {
-        const int c = tc / p.chunk;
+      if (dvalid && tc < L && (p.chunk == kS || (half == 0 && tck == 0))) {
+        const int c = p.chunk == kS ? tc / kS : tc / p.chunk;
 #pragma unroll
         for (int j = 0; j < CPT; ++j)
           *reinterpret_cast<float4*>(p.ckpt + (((size_t)b * p.nchunks + c) * p.D + dg + j) * N + n0) =
@@ -383,6 +399,8 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
     }
     __syncthreads();
     if (tid == 0 && k + kNST < nitems) issue(k + kNST);
+    tck += kTT;
+    if (tck >= p.chunk) tck -= p.chunk;
 
     if (ti == ntiles - 1 && te == L && p.h_last != nullptr && dvalid) {
 #pragma unroll
