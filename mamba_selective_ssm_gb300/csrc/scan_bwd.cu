@@ -50,6 +50,8 @@ struct BwdSmem {
   alignas(16) float dlt_f[kTT * DT];
   alignas(16) float dx_f[kTT * DT];  // delta * x
   alignas(16) float ds_f[kTT * DT];  // dy * silu(z)
+  alignas(16) float x_f[kTT * DT];   // x
+  alignas(16) float gz_f[kTT * DT];  // dy * silu'(z) = dy * sig(z) * (1 + z (1 - sig(z)))
   alignas(16) float B_f[kTT * N];
   alignas(16) float C_f[kTT * N];
   // one 8-step window's per-lane shares
@@ -424,6 +426,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
         reinterpret_cast<float4*>(S.B_f)[gi] = make_float4(bv[0], bv[1], bv[2], bv[3]);
       }
       __syncthreads();
+      if (tid == 0 && k + NSTG < nitems) issue(k + NSTG);
 #pragma unroll
       for (int half = 0; half < kTT / kS; ++half) {
         tmem_st8(tlane + (uint32_t)((tl * (kTT / kS) + half) * 8),
@@ -456,7 +459,6 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
       }
       if (lastA) tmem_wait_st();  // the chunk's states are parked before pass B reads them
       __syncthreads();
-      if (tid == 0 && k + NSTG < nitems) issue(k + NSTG);
       continue;
     }
 
@@ -473,20 +475,26 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    // widen the tile once: everything the windows and their epilogues read is
+    // fp32 in shared memory, so the staging slot is free after this pass
     for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
-      float dv[4], xv[4], zv[4], gv[4];
+      float dv[4], xv[4], zv[4], gv[4], dxv[4], dsv[4], gzv[4];
       AT::ld4(&S.dlt[slot][gi * 4], dv);
       AT::ld4(&S.x[slot][gi * 4], xv);
       AT::ld4(&S.z[slot][gi * 4], zv);
       AT::ld4(&S.dy[slot][gi * 4], gv);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        xv[e] *= dv[e];
-        gv[e] *= zv[e] * sigmoid(zv[e]);
+        const float sg = sigmoid(zv[e]);
+        dxv[e] = xv[e] * dv[e];
+        dsv[e] = gv[e] * (zv[e] * sg);
+        gzv[e] = gv[e] * sg * fmaf(zv[e], 1.0f - sg, 1.0f);
       }
       reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
-      reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(xv[0], xv[1], xv[2], xv[3]);
-      reinterpret_cast<float4*>(S.ds_f)[gi] = make_float4(gv[0], gv[1], gv[2], gv[3]);
+      reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(dxv[0], dxv[1], dxv[2], dxv[3]);
+      reinterpret_cast<float4*>(S.ds_f)[gi] = make_float4(dsv[0], dsv[1], dsv[2], dsv[3]);
+      reinterpret_cast<float4*>(S.x_f)[gi] = make_float4(xv[0], xv[1], xv[2], xv[3]);
+      reinterpret_cast<float4*>(S.gz_f)[gi] = make_float4(gzv[0], gzv[1], gzv[2], gzv[3]);
     }
     for (int gi = tid; gi < kTT * N / 4; gi += G::NT) {
       float bv[4], cv[4];
@@ -496,6 +504,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
       reinterpret_cast<float4*>(S.C_f)[gi] = make_float4(cv[0], cv[1], cv[2], cv[3]);
     }
     __syncthreads();
+    if (tid == 0 && k + NSTG < nitems) issue(k + NSTG);
 
     for (int sub = kTT / kS - 1; sub >= 0; --sub) {
       const int sb = tl * (kTT / kS) + sub;
@@ -604,16 +613,18 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
       for (int e = tid; e < kS * N / 2; e += G::NT) {  // (row, dB | dC, group of 4 states)
         const int i = e / (N / 2), qq = (e % (N / 2)) / (N / 4), n4 = (e % (N / 4)) * 4;
         const int t = t0 + sub * kS + i;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float2 a01 = f2(0.f, 0.f), a23 = f2(0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < G::W; ++w)
 #pragma unroll
           for (int c = 0; c < G::CG; ++c) {
             const float4 v = *reinterpret_cast<const float4*>(&S.dbc[w][i][qq][c * N + n4]);
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            a01 = add2(a01, f2(v.x, v.y));
+            a23 = add2(a23, f2(v.z, v.w));
           }
         if (t < L)
-          *reinterpret_cast<float4*>(&p.ws_dBC[(((size_t)blockIdx.x * p.B + b) * L + t) * (2 * N) + qq * N + n4]) = acc;
+          *reinterpret_cast<float4*>(&p.ws_dBC[(((size_t)blockIdx.x * p.B + b) * L + t) * (2 * N) + qq * N + n4]) =
+              make_float4(a01.x, a01.y, a23.x, a23.y);
       }
       // per-(t, d) gradients, four channels per thread
       for (int gi = tid; gi < kS * DT / 4; gi += G::NT) {
@@ -621,37 +632,43 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
         const int rr = sub * kS + i;
         const int t = t0 + rr, d = d0 + c4;
         if (t < L && d < p.D) {
-          float dv[4], xv[4], zv[4], gv[4], o0[4], o1[4], o2[4];
-          AT::ld4(&S.dlt[slot][rr * DT + c4], dv);
-          AT::ld4(&S.x[slot][rr * DT + c4], xv);
-          AT::ld4(&S.z[slot][rr * DT + c4], zv);
-          AT::ld4(&S.dy[slot][rr * DT + c4], gv);
-          float4 sv = *reinterpret_cast<const float4*>(&S.sp[i][0][c4]);
-          float4 ab0 = *reinterpret_cast<const float4*>(&S.sab[i][0][2 * c4]);
-          float4 ab1 = *reinterpret_cast<const float4*>(&S.sab[i][0][2 * c4 + 4]);
+          float o0[4], o1[4], o2[4];
+          const float4 s4 = *reinterpret_cast<const float4*>(&S.sp[i][0][c4]);
+          const float4 a4 = *reinterpret_cast<const float4*>(&S.sab[i][0][2 * c4]);
+          const float4 b4 = *reinterpret_cast<const float4*>(&S.sab[i][0][2 * c4 + 4]);
+          float2 s01 = f2(s4.x, s4.y), s23 = f2(s4.z, s4.w);
+          float2 ab00 = f2(a4.x, a4.y), ab01 = f2(a4.z, a4.w), ab10 = f2(b4.x, b4.y), ab11 = f2(b4.z, b4.w);
 #pragma unroll
           for (int g = 1; g < N / 4; ++g) {
             const float4 u = *reinterpret_cast<const float4*>(&S.sp[i][g][c4]);
             const float4 v0 = *reinterpret_cast<const float4*>(&S.sab[i][g][2 * c4]);
             const float4 v1 = *reinterpret_cast<const float4*>(&S.sab[i][g][2 * c4 + 4]);
-            sv.x += u.x; sv.y += u.y; sv.z += u.z; sv.w += u.w;
-            ab0.x += v0.x; ab0.y += v0.y; ab0.z += v0.z; ab0.w += v0.w;
-            ab1.x += v1.x; ab1.y += v1.y; ab1.z += v1.z; ab1.w += v1.w;
+            s01 = add2(s01, f2(u.x, u.y));
+            s23 = add2(s23, f2(u.z, u.w));
+            ab00 = add2(ab00, f2(v0.x, v0.y));
+            ab01 = add2(ab01, f2(v0.z, v0.w));
+            ab10 = add2(ab10, f2(v1.x, v1.y));
+            ab11 = add2(ab11, f2(v1.z, v1.w));
           }
+          const float4 dv4 = *reinterpret_cast<const float4*>(&S.dlt_f[rr * DT + c4]);
+          const float4 xv4 = *reinterpret_cast<const float4*>(&S.x_f[rr * DT + c4]);
           const float4 dsv = *reinterpret_cast<const float4*>(&S.ds_f[rr * DT + c4]);
+          const float4 gz4 = *reinterpret_cast<const float4*>(&S.gz_f[rr * DT + c4]);
           const float4 Dd4 = *reinterpret_cast<const float4*>(&S.Dv_s[c4]);
-          const float shv[4] = {sv.x, sv.y, sv.z, sv.w};
-          const float sAv[4] = {ab0.x, ab0.z, ab1.x, ab1.z};
-          const float sBv[4] = {ab0.y, ab0.w, ab1.y, ab1.w};
+          const float shv[4] = {s01.x, s01.y, s23.x, s23.y};
+          const float sAv[4] = {ab00.x, ab01.x, ab10.x, ab11.x};
+          const float sBv[4] = {ab00.y, ab01.y, ab10.y, ab11.y};
+          const float dv[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+          const float xv[4] = {xv4.x, xv4.y, xv4.z, xv4.w};
+          const float gz[4] = {gz4.x, gz4.y, gz4.z, gz4.w};
           const float dsa[4] = {dsv.x, dsv.y, dsv.z, dsv.w};
           const float Dd[4] = {Dd4.x, Dd4.y, Dd4.z, Dd4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float sg = sigmoid(zv[e]);
             const float s = fmaf(Dd[e], xv[e], shv[e]);
-            o0[e] = fmaf(dsa[e], Dd[e], dv[e] * sBv[e]);                 // dx
-            o1[e] = fmaf(sAv[e], kLn2, xv[e] * sBv[e]);                  // ddelta
-            o2[e] = gv[e] * s * sg * fmaf(zv[e], 1.0f - sg, 1.0f);     // dz
+            o0[e] = fmaf(dsa[e], Dd[e], dv[e] * sBv[e]);  // dx
+            o1[e] = fmaf(sAv[e], kLn2, xv[e] * sBv[e]);   // ddelta
+            o2[e] = gz[e] * s;                             // dz
             dDacc[e] = fmaf(dsa[e], xv[e], dDacc[e]);
           }
           const size_t off = ((size_t)b * L + t) * p.D + d;
@@ -662,7 +679,6 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
       }
       __syncthreads();
     }
-    if (tid == 0 && k + NSTG < nitems) issue(k + NSTG);
 
     if (t0 == 0 && p.dh0 != nullptr && dvalid) {  // last item of batch row b: ga = a_0 G_0
 #pragma unroll
@@ -756,10 +772,11 @@ inline BwdPlan make_plan(int B, int L, int D, int N, int chunk) {
   return pl;
 }
 
-// pipeline depth: fp32 tiles are twice the size of bf16 ones
+// pipeline depth: a staging slot is released right after the tile's widening
+// pass, so two slots keep one tile in flight during the tile's windows
 template <typename T>
 struct Stages {
-  static constexpr int value = sizeof(T) == 4 ? 2 : 3;
+  static constexpr int value = 2;
 };
 
 template <int N, typename T, int NSTG = Stages<T>::value, int DT = bwd_dt<N>()>
