@@ -4,12 +4,16 @@
 // the sequence in tiles of TT = 16 steps that TMA stages into shared memory
 // ([TT x DT] boxes of delta, x, z, dy; [TT*N] boxes of B_t, C_t).
 //
-// Inside a warp, lane = cg * NG + ng: the NG = N/4 lanes of channel-pair group
-// cg share two channels and split the N states four apiece, so every thread
-// advances 2 channels x 4 states = 8 (d, n) recurrences with packed f32x2
-// arithmetic.  Sums over n (y, and the delta / x gradients) are reduce-scatters
-// across the NG lanes of a pair group (lane bits below log2 NG); sums over d
-// (dB, dC) run across the pair groups and the warps of the CTA.
+// Backward: inside a warp, lane = cg * NG + ng: the NG = N/4 lanes of
+// channel-pair group cg share two channels and split the N states four apiece,
+// so every thread advances 2 channels x 4 states = 8 (d, n) recurrences with
+// packed f32x2 arithmetic.  Sums over n (y, and the delta / x gradients) add
+// the NG lanes' shares in shared memory; sums over d (dB, dC) run across the
+// pair groups and the warps of the CTA.
+// Forward: 1 channel x 4 states per thread with lane = ng * CG + cg, so that
+// the CG lanes reading the same four B_t / C_t values are consecutive: a
+// 128-bit shared load whose lanes share addresses in runs of 8 costs two
+// wavefronts, against four when the sharing lanes are interleaved.
 #pragma once
 
 #include "common.cuh"

@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_summary_kernel(
   extern __shared__ __align__(128) unsigned char smem_raw[];
   FwdSumSmem<T, N, DT>& S = *reinterpret_cast<FwdSumSmem<T, N, DT>*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ng = lane % G::NG, cg = lane / G::NG;
+  const int ng = lane / G::CG, cg = lane % G::CG;
   const int dl = warp * G::WC + cg * CPT;
   const int d0 = blockIdx.x * DT;
   const int dg = d0 + dl;
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
   FwdSmem<T, N, DT>& S = *reinterpret_cast<FwdSmem<T, N, DT>*>(smem_raw);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ng = lane % G::NG, cg = lane / G::NG;
+  const int ng = lane / G::CG, cg = lane % G::CG;
   const int dl = warp * G::WC + cg * CPT;  // first of the thread's channels, CTA-local
   const int d0 = blockIdx.x * DT;
   const int dg = d0 + dl;
