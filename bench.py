@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--chunk", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip timing the kernels next to the hot path")
     return ap.parse_args()
 
 
@@ -376,6 +377,37 @@ def main():
     scan_ms = per_call["scan_fwd"] + per_call["scan_bwd"]
     scan_bytes = alg["scan_fwd"] + alg["scan_bwd"]
 
+    # ---- the producers and fusions next to the hot path, each timed alone on the same tensors
+    nxt = {}
+    if not args.no_next:
+        e = 2 if wl.dtype == "bf16" else 4
+        c_bias = torch.zeros((D,), **f32)
+        N_ = {"conv_out": torch.empty((B, L, D), device=dev, dtype=tdt), "r_y": torch.empty((B * L, H), device=dev, dtype=tdt),
+              "r_rms": torch.empty((B * L,), **f32)}
+        extra = {
+            "conv1d_silu_fwd": (lambda: lib.conv1d_causal_fwd(p(X["c_x"]), p(X["c_w"]), p(c_bias), p(N_["conv_out"]),
+                                                              B, L, D, K, 1, sdt, sp), 2 * elems * e),
+            "conv1d_silu_bwd": (lambda: lib.conv1d_causal_silu_bwd(p(X["c_dout"]), p(X["c_x"]), p(X["c_w"]), p(c_bias),
+                                                                   p(O["c_dx"]), p(O["c_dw"]), p(O["c_db"]), B, L, D, K,
+                                                                   sdt, p(W), wsz, sp), elems * (8 + e)),
+            "rmsnorm_fwd": (lambda: lib.rmsnorm_fwd(p(X["r_x"]), p(X["r_scale"]), ctypes.c_float(1e-5), p(N_["r_y"]),
+                                                    p(N_["r_rms"]), B * L, H, sdt, sp), B * L * (2 * H * e + 4)),
+        }
+        for n, (fn, nbytes) in extra.items():
+            for _ in range(3):
+                if fn() != 0:
+                    raise RuntimeError(f"{n} failed")
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            iters = 20
+            a0.record(stream)
+            for _ in range(iters):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = a0.elapsed_time(a1) / iters
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            nxt[n] = {"ms": round(ms, 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+
     # ---- end to end through the public API: pinned host inputs in, results out, every step
     e2e = None
     if not args.no_e2e:
@@ -431,7 +463,7 @@ def main():
             "scan_fwd_bwd": {"ms": round(scan_ms, 5), "elems_per_s": elems / (scan_ms * 1e-3),
                              "alg_GB/s": round(scan_bytes / (scan_ms * 1e-3) / 1e9, 1),
                              "frac": round(scan_bytes / (scan_ms * 1e-3) / 1e9 / peak, 4)},
-            "kernels": kern, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+            "kernels": kern, "next_kernels": nxt or None, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps,
         }), flush=True)
     if ws > 1:

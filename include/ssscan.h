@@ -162,6 +162,21 @@ int conv1d_causal_bwd(const float* dout, const void* x, const float* w,
                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * conv1d_causal_silu_bwd — conv1d_causal_bwd fused with the SiLU backward of
+ * the conv -> SiLU branch (see conv1d_causal_fwd with silu = 1): given
+ *   dact : [B, L, D] fp32, dL/d(silu(pre)),
+ * it forms g = dact * silu'(pre) with pre = bias + sum_k w[k] x[t-(d_conv-1)+k]
+ * recomputed from x, w and bias (NULL: zero), silu'(v) = s (1 + v (1 - s)),
+ * s = sigmoid(v), and then writes / accumulates dx, dw, db exactly as
+ * conv1d_causal_bwd does with dout = g (db is the bias gradient).  Same
+ * workspace (conv1d_causal_bwd_workspace_size), sizes and alignment rules;
+ * bias 16-byte aligned when given.
+ */
+int conv1d_causal_silu_bwd(const float* dact, const void* x, const float* w, const float* bias,
+                           float* dx, float* dw, float* db, int B, int L, int D, int d_conv, int x_dtype,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Workspace bytes rmsnorm_bwd needs (0 on invalid sizes).
  */
 size_t rmsnorm_bwd_workspace_size(int rows, int dim);
@@ -207,6 +222,36 @@ int rmsnorm_bwd(const void* dy, const void* x, const float* scale, const float* 
  */
 int rmsnorm_bwd_noalloc(const void* dy, const void* x, const float* scale, const float* rms,
                         float* dx, float* dscale, int rows, int dim, int dtype, void* stream);
+
+/*
+ * conv1d_causal_fwd — the depthwise causal conv1d that conv1d_causal_bwd
+ * differentiates, with an optional SiLU on its output (the conv -> SiLU branch
+ * in front of the scan).  The pages give only the backward (mamba-rs
+ * backward_ops.rs, backward_conv1d_step, whose shift register fixes the tap
+ * order: newest input at tap d_conv-1); this is the operation it inverts:
+ *   pre[b,t,d] = bias[d] + sum_k w[d,k] * x[b, t-(d_conv-1)+k, d]      (x at t<0 is 0)
+ *   out[b,t,d] = silu ? pre * sigmoid(pre) : pre
+ *   x    : [B, L, D] (x_dtype: SS_F32 or SS_BF16)
+ *   out  : [B, L, D] same dtype, overwritten (bf16 rounded to nearest even)
+ *   w    : [D, d_conv] fp32;  bias : [D] fp32, or NULL for zero
+ * d_conv in 1..4; D a multiple of 8; x, out and bias 16-byte aligned.
+ */
+int conv1d_causal_fwd(const void* x, const float* w, const float* bias, void* out,
+                      int B, int L, int D, int d_conv, int silu, int x_dtype, void* stream);
+
+/*
+ * rmsnorm_fwd — RMSNorm forward, producing the root mean square that
+ * rmsnorm_bwd takes (mamba-rs backward_ops.rs, backward_rms_norm receives the
+ * saved rms itself):
+ *   rms[r]   = sqrt(mean_i x[r,i]^2 + eps)
+ *   y[r,i]   = x[r,i] * scale[i] / rms[r]
+ *   x, y  : [rows, dim] (dtype; y overwritten, bf16 rounded to nearest even)
+ *   scale : [dim] fp32;  rms : [rows] fp32 output, or NULL
+ * dim a multiple of 8 and at most 32768; eps >= 0 (else SS_ERR_DIM);
+ * x, y, scale and rms 16-byte aligned.
+ */
+int rmsnorm_fwd(const void* x, const float* scale, float eps, void* y, float* rms,
+                int rows, int dim, int dtype, void* stream);
 
 /*
  * ss_device_status — synchronises `stream`, then reads and clears the

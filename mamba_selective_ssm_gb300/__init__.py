@@ -1,6 +1,7 @@
 """GB300-native Mamba selective scan: forward and backward of the diagonal
-selective SSM, the depthwise causal conv1d backward and the RMSNorm backward,
-as hand-written sm_103a CUDA kernels behind the C ABI in include/ssscan.h.
+selective SSM, the depthwise causal conv1d (+SiLU) and RMSNorm forward and
+backward, as hand-written sm_103a CUDA kernels behind the C ABI in
+include/ssscan.h.
 
 The Python layer only checks arguments, allocates outputs with PyTorch and
 calls the library on the current CUDA stream.
@@ -8,10 +9,10 @@ calls the library on the current CUDA stream.
 
 from ._build import build
 from ._capi import SSError, load
-from .ops import (conv1d_causal_bwd, device_status, num_chunks, rmsnorm_bwd, scan_bwd_workspace_size, ss_scan_bwd,
-                  ss_scan_fwd)
+from .ops import (conv1d_causal_bwd, conv1d_causal_fwd, conv1d_causal_silu_bwd, device_status, num_chunks, rmsnorm_bwd, rmsnorm_fwd,
+                  scan_bwd_workspace_size, scan_fwd_workspace_size, ss_scan_bwd, ss_scan_fwd)
 
 __all__ = [
-    "build", "load", "SSError", "ss_scan_fwd", "ss_scan_bwd", "scan_bwd_workspace_size", "conv1d_causal_bwd",
-    "rmsnorm_bwd", "num_chunks", "device_status",
+    "build", "load", "SSError", "ss_scan_fwd", "ss_scan_bwd", "scan_fwd_workspace_size", "scan_bwd_workspace_size",
+    "conv1d_causal_fwd", "conv1d_causal_bwd", "conv1d_causal_silu_bwd", "rmsnorm_fwd", "rmsnorm_bwd", "num_chunks", "device_status",
 ]

@@ -36,9 +36,12 @@ SIGNATURES = {
     "ss_scan_bwd": (_i, [_vp] * 18 + [_i] * 6 + [_vp, _sz, _vp]),
     "conv1d_causal_bwd_workspace_size": (_sz, [_i] * 4),
     "conv1d_causal_bwd": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _sz, _vp]),
+    "conv1d_causal_silu_bwd": (_i, [_vp] * 7 + [_i] * 5 + [_vp, _sz, _vp]),
     "rmsnorm_bwd_workspace_size": (_sz, [_i, _i]),
     "rmsnorm_bwd": (_i, [_vp] * 6 + [_i] * 3 + [_vp, _sz, _vp]),
     "rmsnorm_bwd_noalloc": (_i, [_vp] * 6 + [_i] * 3 + [_vp]),
+    "conv1d_causal_fwd": (_i, [_vp] * 4 + [_i] * 6 + [_vp]),
+    "rmsnorm_fwd": (_i, [_vp, _vp, ctypes.c_float, _vp, _vp, _i, _i, _i, _vp]),
     "ss_device_status": (_i, [_vp]),
 }
 

@@ -11,6 +11,11 @@
 // in registers, and writes one partial per CTA row; colsum_kernel adds
 // the partials in fixed order into dw / db.  HBM traffic is one read of dout
 // and x plus one write of dx (the K-1 halo steps per tile come from L2).
+//
+// conv1d_causal_silu_bwd takes the gradient after a SiLU on the conv output
+// instead: the x window then reaches K-1 steps ahead as well, so that each
+// incoming dout[t] is turned into g[t] = dout[t] * silu'(pre[t]), with
+// pre[t] = bias + sum_k w[k] x[t-(K-1)+k] recomputed from x and w.
 #include "common.cuh"
 
 namespace {
@@ -36,10 +41,16 @@ __device__ __forceinline__ float4 f4fma(float4 a, float4 b, float4 c) {
 __device__ __forceinline__ float4 f4add(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 __device__ __forceinline__ float4 f4z() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
-template <int K, typename T>
+__device__ __forceinline__ float dsilu(float v) {
+  const float sg = sigmoid(v);
+  return sg * fmaf(v, 1.0f - sg, 1.0f);
+}
+
+template <int K, typename T, bool SILU>
 __global__ void __launch_bounds__(kCThreads) conv_bwd_kernel(const float* __restrict__ dout, const T* __restrict__ x,
-                                                             const float* __restrict__ w, float* __restrict__ dx,
-                                                             float* __restrict__ ws, int B, int L, int D) {
+                                                             const float* __restrict__ w, const float* __restrict__ bias,
+                                                             float* __restrict__ dx, float* __restrict__ ws, int B, int L,
+                                                             int D) {
   const int d = (blockIdx.x * kCThreads + threadIdx.x) * 4;
   const bool valid = d < D;  // D % 8 == 0, so all four channels are in range
   const int ntt = (L + kCTile - 1) / kCTile;
@@ -52,8 +63,52 @@ __global__ void __launch_bounds__(kCThreads) conv_bwd_kernel(const float* __rest
   float4 dw[K], db = f4z();
 #pragma unroll
   for (int k = 0; k < K; ++k) dw[k] = f4z();
+  const float4 b4 = (SILU && valid && bias != nullptr) ? *reinterpret_cast<const float4*>(bias + d) : f4z();
+  // g[t] = dout[t] * silu'(pre[t]); xs points at x[t-(K-1)] .. x[t]
+  auto gact = [&](float4 g, const float4* xs) {
+    float4 pre = b4;
+#pragma unroll
+    for (int k = 0; k < K; ++k) pre = f4fma(wk[k], xs[k], pre);
+    return make_float4(g.x * dsilu(pre.x), g.y * dsilu(pre.y), g.z * dsilu(pre.z), g.w * dsilu(pre.w));
+  };
 
-  if (valid) {
+  if (valid && SILU) {
+    for (int bt = blockIdx.y; bt < B * ntt; bt += gridDim.y) {
+      const int b = bt / ntt, t0 = (bt % ntt) * kCTile;
+      const int t1 = min(L, t0 + kCTile);
+      const float* g = dout + (size_t)b * L * D + d;
+      const T* xb = x + (size_t)b * L * D + d;
+      float4 gw[K];          // gw[j] = g[s+j]
+      float4 xa[2 * K - 1];  // xa[j] = x[s-(K-1)+j]: K-1 steps behind to K-1 ahead
+#pragma unroll
+      for (int j = 0; j < 2 * K - 2; ++j) {
+        const int tx = t0 - (K - 1) + j;
+        xa[j + 1] = (tx >= 0 && tx < L) ? ld_x4(xb + (size_t)tx * D) : f4z();
+      }
+#pragma unroll
+      for (int j = 0; j < K - 1; ++j) {
+        const int t = t0 + j;
+        gw[j + 1] = t < L ? gact(*reinterpret_cast<const float4*>(g + (size_t)t * D), &xa[j + 1]) : f4z();
+      }
+#pragma unroll 2
+      for (int s = t0; s < t1; ++s) {
+#pragma unroll
+        for (int j = 0; j < 2 * K - 2; ++j) xa[j] = xa[j + 1];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) gw[j] = gw[j + 1];
+        const int tg = s + K - 1;
+        xa[2 * K - 2] = tg < L ? ld_x4(xb + (size_t)tg * D) : f4z();
+        gw[K - 1] = tg < L ? gact(*reinterpret_cast<const float4*>(g + (size_t)tg * D), &xa[K - 1]) : f4z();
+        float4 acc = f4z();
+#pragma unroll
+        for (int j = 0; j < K; ++j) acc = f4fma(gw[j], wk[K - 1 - j], acc);
+        *reinterpret_cast<float4*>(dx + ((size_t)b * L + s) * D + d) = acc;
+#pragma unroll
+        for (int k = 0; k < K; ++k) dw[k] = f4fma(gw[0], xa[k], dw[k]);
+        db = f4add(db, gw[0]);
+      }
+    }
+  } else if (valid) {
     for (int bt = blockIdx.y; bt < B * ntt; bt += gridDim.y) {
       const int b = bt / ntt, t0 = (bt % ntt) * kCTile;
       const int t1 = min(L, t0 + kCTile);
@@ -86,6 +141,8 @@ __global__ void __launch_bounds__(kCThreads) conv_bwd_kernel(const float* __rest
         db = f4add(db, gw[0]);
       }
     }
+  }
+  if (valid) {
     float* o = ws + (size_t)blockIdx.y * (K + 1) * D + d;  // partial row: [K+1][D]
 #pragma unroll
     for (int k = 0; k < K; ++k) *reinterpret_cast<float4*>(o + (size_t)k * D) = dw[k];
@@ -130,10 +187,11 @@ int conv_validate(int B, int L, int D, int K, int x_dtype) {
   return SS_OK;
 }
 
-template <int K, typename T>
-int conv_launch(const float* dout, const void* x, const float* w, float* dx, float* dw, float* db, int B, int L, int D,
-                float* ws, const ConvPlan& pl, cudaStream_t s) {
-  conv_bwd_kernel<K, T><<<dim3(pl.gx, pl.gy), kCThreads, 0, s>>>(dout, static_cast<const T*>(x), w, dx, ws, B, L, D);
+template <int K, typename T, bool SILU>
+int conv_launch(const float* dout, const void* x, const float* w, const float* bias, float* dx, float* dw, float* db,
+                int B, int L, int D, float* ws, const ConvPlan& pl, cudaStream_t s) {
+  conv_bwd_kernel<K, T, SILU>
+      <<<dim3(pl.gx, pl.gy), kCThreads, 0, s>>>(dout, static_cast<const T*>(x), w, bias, dx, ws, B, L, D);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
   return colsum(ws, (long long)D * (K + 1), pl.gy, ConvStore{dw, db, D, K}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
@@ -145,31 +203,47 @@ extern "C" size_t conv1d_causal_bwd_workspace_size(int B, int L, int D, int d_co
   return conv_plan(B, L, D, d_conv).bytes;
 }
 
-extern "C" int conv1d_causal_bwd(const float* dout, const void* x, const float* w, float* dx, float* dw, float* db, int B,
-                                 int L, int D, int d_conv, int x_dtype, void* workspace, size_t ws_bytes, void* stream) {
+namespace {
+
+template <typename T, bool SILU>
+int conv_dispatch(const float* dout, const void* x, const float* w, const float* bias, float* dx, float* dw, float* db,
+                  int B, int L, int D, int K, float* ws, const ConvPlan& pl, cudaStream_t s) {
+  switch (K) {
+    case 1: return conv_launch<1, T, SILU>(dout, x, w, bias, dx, dw, db, B, L, D, ws, pl, s);
+    case 2: return conv_launch<2, T, SILU>(dout, x, w, bias, dx, dw, db, B, L, D, ws, pl, s);
+    case 3: return conv_launch<3, T, SILU>(dout, x, w, bias, dx, dw, db, B, L, D, ws, pl, s);
+    default: return conv_launch<4, T, SILU>(dout, x, w, bias, dx, dw, db, B, L, D, ws, pl, s);
+  }
+}
+
+template <bool SILU>
+int conv_bwd_entry(const float* dout, const void* x, const float* w, const float* bias, float* dx, float* dw, float* db,
+                   int B, int L, int D, int d_conv, int x_dtype, void* workspace, size_t ws_bytes, void* stream) {
   if (!dout || !x || !w || !dx || !dw || !db) return SS_ERR_NULL;
   const int v = conv_validate(B, L, D, d_conv, x_dtype);
   if (v != SS_OK) return v;
   const void* ptrs[] = {dout, x, w, dx, dw, db};
   for (const void* q : ptrs)
     if (!ssh::aligned16(q)) return SS_ERR_ALIGN;
+  if (bias && !ssh::aligned16(bias)) return SS_ERR_ALIGN;
   const ConvPlan pl = conv_plan(B, L, D, d_conv);
   if (workspace == nullptr || ws_bytes < pl.bytes) return SS_ERR_WORKSPACE;
   if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
   float* ws = static_cast<float*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (x_dtype == SS_F32) {
-    switch (d_conv) {
-      case 1: return conv_launch<1, float>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
-      case 2: return conv_launch<2, float>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
-      case 3: return conv_launch<3, float>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
-      default: return conv_launch<4, float>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
-    }
-  }
-  switch (d_conv) {
-    case 1: return conv_launch<1, __nv_bfloat16>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
-    case 2: return conv_launch<2, __nv_bfloat16>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
-    case 3: return conv_launch<3, __nv_bfloat16>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
-    default: return conv_launch<4, __nv_bfloat16>(dout, x, w, dx, dw, db, B, L, D, ws, pl, s);
-  }
+  if (x_dtype == SS_F32) return conv_dispatch<float, SILU>(dout, x, w, bias, dx, dw, db, B, L, D, d_conv, ws, pl, s);
+  return conv_dispatch<__nv_bfloat16, SILU>(dout, x, w, bias, dx, dw, db, B, L, D, d_conv, ws, pl, s);
+}
+
+}  // namespace
+
+extern "C" int conv1d_causal_bwd(const float* dout, const void* x, const float* w, float* dx, float* dw, float* db, int B,
+                                 int L, int D, int d_conv, int x_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  return conv_bwd_entry<false>(dout, x, w, nullptr, dx, dw, db, B, L, D, d_conv, x_dtype, workspace, ws_bytes, stream);
+}
+
+extern "C" int conv1d_causal_silu_bwd(const float* dact, const void* x, const float* w, const float* bias, float* dx,
+                                      float* dw, float* db, int B, int L, int D, int d_conv, int x_dtype, void* workspace,
+                                      size_t ws_bytes, void* stream) {
+  return conv_bwd_entry<true>(dact, x, w, bias, dx, dw, db, B, L, D, d_conv, x_dtype, workspace, ws_bytes, stream);
 }

@@ -9,6 +9,9 @@ Names and argument order follow include/ssscan.h:
   -> dict of gradients
 * ``conv1d_causal_bwd(dout, x, w, dw=None, db=None)`` -> ``(dx, dw, db)``
 * ``rmsnorm_bwd(dy, x, scale, rms, dscale=None)`` -> ``(dx, dscale)``
+* ``conv1d_causal_fwd(x, w, bias=None, silu=False)`` -> ``out``
+* ``conv1d_causal_silu_bwd(dact, x, w, bias=None, dw=None, db=None)`` -> ``(dx, dw, db)``
+* ``rmsnorm_fwd(x, scale, eps)`` -> ``(y, rms)``
 
 Activations are ``torch.float32`` or ``torch.bfloat16`` CUDA tensors, contiguous;
 parameters, states and gradients are ``torch.float32``.
@@ -156,6 +159,30 @@ def conv1d_causal_bwd(dout, x, w, dw=None, db=None, workspace=None):
     return dx, dw, db
 
 
+def conv1d_causal_silu_bwd(dact, x, w, bias=None, dw=None, db=None, workspace=None):
+    """Backward through silu(conv1d(x) + bias) given dL/d(silu output); dw, db accumulate."""
+    lib = load()
+    B, L, D = x.shape
+    K = w.shape[1]
+    dev = x.device
+    xdt = _act_dtype(x)
+    _req(dact, "dact", (B, L, D), torch.float32, dev)
+    _req(x, "x", (B, L, D), x.dtype, dev)
+    _req(w, "w", (D, K), torch.float32, dev)
+    if bias is not None:
+        _req(bias, "bias", (D,), torch.float32, dev)
+    dw = torch.zeros((D, K), device=dev, dtype=torch.float32) if dw is None else _req(dw, "dw", (D, K), torch.float32, dev)
+    db = torch.zeros((D,), device=dev, dtype=torch.float32) if db is None else _req(db, "db", (D,), torch.float32, dev)
+    dx = torch.empty((B, L, D), device=dev, dtype=torch.float32)
+    ws_bytes = lib.conv1d_causal_bwd_workspace_size(B, L, D, K)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), device=dev, dtype=torch.uint8)
+    rc = lib.conv1d_causal_silu_bwd(_p(dact), _p(x), _p(w), _p(bias), _p(dx), _p(dw), _p(db), B, L, D, K, xdt,
+                                    _p(workspace), workspace.numel() * workspace.element_size(), _stream())
+    check(rc, "conv1d_causal_silu_bwd")
+    return dx, dw, db
+
+
 def rmsnorm_bwd(dy, x, scale, rms, dscale=None, workspace=None):
     lib = load()
     R, H = x.shape
@@ -175,6 +202,38 @@ def rmsnorm_bwd(dy, x, scale, rms, dscale=None, workspace=None):
                          workspace.numel() * workspace.element_size(), _stream())
     check(rc, "rmsnorm_bwd")
     return dx, dscale
+
+
+def conv1d_causal_fwd(x, w, bias=None, silu: bool = False, out=None):
+    """Depthwise causal conv1d (+ optional SiLU); ``out`` has x's dtype."""
+    lib = load()
+    B, L, D = x.shape
+    K = w.shape[1]
+    dev = x.device
+    xdt = _act_dtype(x)
+    _req(x, "x", (B, L, D), x.dtype, dev)
+    _req(w, "w", (D, K), torch.float32, dev)
+    if bias is not None:
+        _req(bias, "bias", (D,), torch.float32, dev)
+    out = torch.empty_like(x) if out is None else _req(out, "out", (B, L, D), x.dtype, dev)
+    rc = lib.conv1d_causal_fwd(_p(x), _p(w), _p(bias), _p(out), B, L, D, K, int(bool(silu)), xdt, _stream())
+    check(rc, "conv1d_causal_fwd")
+    return out
+
+
+def rmsnorm_fwd(x, scale, eps: float, want_rms: bool = True):
+    """RMSNorm forward: ``(y, rms)`` with y in x's dtype and rms fp32 (None unless ``want_rms``)."""
+    lib = load()
+    R, H = x.shape
+    dev = x.device
+    dt = _act_dtype(x)
+    _req(x, "x", (R, H), x.dtype, dev)
+    _req(scale, "scale", (H,), torch.float32, dev)
+    y = torch.empty_like(x)
+    rms = torch.empty((R,), device=dev, dtype=torch.float32) if want_rms else None
+    rc = lib.rmsnorm_fwd(_p(x), _p(scale), float(eps), _p(y), _p(rms), R, H, dt, _stream())
+    check(rc, "rmsnorm_fwd")
+    return y, rms
 
 
 def device_status() -> int:

@@ -45,6 +45,17 @@ def conv1d_causal_fwd_ref(x, w, bias=None):
     return out
 
 
+def silu_ref(v):
+    """SiLU, the activation after the conv: v * sigmoid(v) = v / (1 + exp(-v)), float64."""
+    v = np.asarray(v, np.float64)
+    return v / (1.0 + np.exp(-v))
+
+
+def conv1d_causal_silu_fwd_ref(x, w, bias=None):
+    """The conv -> SiLU branch: silu(conv1d_causal_fwd_ref(x, w, bias))."""
+    return silu_ref(conv1d_causal_fwd_ref(x, w, bias))
+
+
 def conv1d_causal_bwd_ref(dout, x, w):
     """Returns (dx [B,L,D], dw [D,K], db [D]) for the loss sum(out * dout)."""
     dout = np.asarray(dout, np.float64)
@@ -62,6 +73,23 @@ def conv1d_causal_bwd_ref(dout, x, w):
         dw[:, k] = np.sum(dout * _state(x, k, K), axis=(0, 1))
     db = np.sum(dout, axis=(0, 1))
     return dx, dw, db
+
+
+def dsilu_ref(v):
+    """d/dv silu(v) = s (1 + v (1 - s)), s = 1 / (1 + exp(-v)), float64."""
+    v = np.asarray(v, np.float64)
+    s = 1.0 / (1.0 + np.exp(-v))
+    return s * (1.0 + v * (1.0 - s))
+
+
+def conv1d_causal_silu_bwd_ref(dact, x, w, bias=None):
+    """Backward of silu(conv1d_causal_fwd_ref(x, w, bias)) for the loss sum(act * dact).
+
+    Chain rule: the conv receives g = dact * silu'(pre) at its output and
+    conv1d_causal_bwd_ref does the rest; the bias gradient equals db.
+    Returns (dx, dw, db)."""
+    pre = conv1d_causal_fwd_ref(x, w, bias)
+    return conv1d_causal_bwd_ref(np.asarray(dact, np.float64) * dsilu_ref(pre), x, w)
 
 
 def conv1d_step_bwd_ref(d_out, conv_state, w, dw, db):

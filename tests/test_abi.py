@@ -117,6 +117,31 @@ def test_scan_bwd_validation_and_workspace(lib):
     assert call(w=_fake(0x90008)) == c.SS_ERR_ALIGN
 
 
+def test_layer_fwd_validation(lib):
+    from mamba_selective_ssm_gb300 import _capi as c
+    p = [_fake(0x10000 + 256 * i) for i in range(4)]
+    conv = lambda ptrs=p, B=2, L=10, D=16, K=4, silu=1, dt=c.SS_BF16: lib.conv1d_causal_fwd(*ptrs, B, L, D, K, silu, dt, None)
+    q = list(p)
+    q[0] = None
+    assert conv(q) == c.SS_ERR_NULL
+    assert conv(K=5) == c.SS_ERR_UNSUPPORTED
+    assert conv(K=0) == c.SS_ERR_DIM
+    assert conv(D=12) == c.SS_ERR_ALIGN
+    assert conv(dt=3) == c.SS_ERR_UNSUPPORTED
+    q = list(p)
+    q[3] = _fake(0x10008)
+    assert conv(q) == c.SS_ERR_ALIGN
+    r = [_fake(0x20000 + 256 * i) for i in range(4)]
+    rms = lambda eps=1e-5, rows=4, dim=64, dt=c.SS_F32, x=r[0]: lib.rmsnorm_fwd(x, r[1], eps, r[2], r[3], rows, dim, dt, None)
+    assert rms(x=None) == c.SS_ERR_NULL
+    assert rms(eps=-1.0) == c.SS_ERR_DIM
+    assert rms(eps=float("nan")) == c.SS_ERR_DIM
+    assert rms(dim=12) == c.SS_ERR_ALIGN
+    assert rms(dim=32776) == c.SS_ERR_DIM
+    assert rms(rows=0) == c.SS_ERR_DIM
+    assert rms(dt=2) == c.SS_ERR_UNSUPPORTED
+
+
 def test_conv_and_rms_validation(lib):
     from mamba_selective_ssm_gb300 import _capi as c
     assert lib.conv1d_causal_bwd_workspace_size(4, 2048, 4096, 4) > 0

@@ -132,3 +132,79 @@ def test_rmsnorm_rows_independent_and_dscale_sums_rows():
     parts = [rmsnorm_bwd_ref(dy[i : i + 1], x[i : i + 1], scale, rms[i : i + 1]) for i in range(6)]
     np.testing.assert_array_equal(np.concatenate([p[0] for p in parts]), dx)
     np.testing.assert_allclose(sum(p[1] for p in parts), dscale, rtol=1e-13)
+
+
+# ------------------------------------------------------------------ forward producers (conv -> SiLU, RMSNorm)
+
+
+def test_silu_matches_scipy_expit():
+    """silu(v) = v * sigmoid(v), checked against SciPy's logistic function."""
+    special = pytest.importorskip("scipy.special")
+    from oracle import silu_ref
+    v = np.concatenate([np.linspace(-60, 60, 1201), [-1e-8, 0.0, 1e-8]])
+    np.testing.assert_allclose(silu_ref(v), v * special.expit(v), rtol=1e-14, atol=1e-300)
+
+
+def test_silu_limits():
+    from oracle import silu_ref
+    assert silu_ref(0.0) == 0.0
+    assert abs(silu_ref(40.0) - 40.0) < 1e-14 * 40
+    assert abs(silu_ref(-40.0)) < 1e-15
+    # odd part: silu(v) - silu(-v) = v
+    v = np.linspace(-5, 5, 41)
+    np.testing.assert_allclose(silu_ref(v) - silu_ref(-v), v, atol=1e-14)
+
+
+def test_conv_silu_is_silu_of_conv():
+    from oracle import conv1d_causal_silu_fwd_ref, silu_ref
+    rng = np.random.default_rng(70)
+    x, w, b, _ = _conv_inputs(rng, B=2, L=11, D=5, K=4)
+    out = conv1d_causal_fwd_ref(x, w, b)
+    np.testing.assert_array_equal(conv1d_causal_silu_fwd_ref(x, w, b), silu_ref(out))
+
+
+def test_rmsnorm_fwd_rms_is_scaled_euclidean_norm():
+    """eps = 0: rms is |x_r| / sqrt(H) (numpy.linalg.norm), and y with unit scale has unit RMS."""
+    rng = np.random.default_rng(71)
+    x = rng.standard_normal((7, 40))
+    y, rms = rmsnorm_fwd_ref(x, np.ones(40), 0.0)
+    np.testing.assert_allclose(rms, np.linalg.norm(x, axis=1) / np.sqrt(40), rtol=1e-14)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=1)), 1.0, rtol=1e-14)
+    scale = 1 + 0.1 * rng.standard_normal(40)
+    y2, _ = rmsnorm_fwd_ref(x, scale, 0.0)
+    np.testing.assert_allclose(y2, y * scale[None, :], rtol=1e-14)
+
+
+def test_rmsnorm_fwd_eps_enters_under_the_root():
+    x = np.array([[3.0, 4.0]])  # mean square 12.5
+    _, rms = rmsnorm_fwd_ref(x, np.ones(2), 0.5)
+    assert rms[0] == np.sqrt(13.0)
+
+
+def test_dsilu_matches_scipy_expit_derivative():
+    """silu'(v) = expit(v) + v expit(v) (1 - expit(v)), from SciPy's logistic function."""
+    special = pytest.importorskip("scipy.special")
+    from oracle import dsilu_ref
+    v = np.linspace(-30, 30, 601)
+    e = special.expit(v)
+    np.testing.assert_allclose(dsilu_ref(v), e + v * e * (1 - e), rtol=1e-13, atol=1e-300)
+
+
+def test_conv_silu_backward_finite_differences():
+    """Central differences of sum(silu(conv(x, w) + b) * dact) in x, w and the bias."""
+    from oracle import conv1d_causal_silu_bwd_ref, conv1d_causal_silu_fwd_ref
+    rng = np.random.default_rng(72)
+    x, w, b, dact = _conv_inputs(rng, B=2, L=7, D=3, K=4)
+    dx, dw, db = conv1d_causal_silu_bwd_ref(dact, x, w, b)
+    loss = lambda: float(np.sum(conv1d_causal_silu_fwd_ref(x, w, b) * dact))
+    for arr, g in ((x, dx), (w, dw), (b, db)):
+        fd = np.empty_like(arr)
+        for idx in np.ndindex(arr.shape):
+            v0 = arr[idx]
+            arr[idx] = v0 + 1e-6
+            lp = loss()
+            arr[idx] = v0 - 1e-6
+            lm = loss()
+            arr[idx] = v0
+            fd[idx] = (lp - lm) / 2e-6
+        assert max_rel_err(g, fd) < 1e-8

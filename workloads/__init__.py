@@ -6,6 +6,8 @@ backward arithmetic.  Both the float64 oracle and the CUDA path consume what it
 returns, and neither imports the other.
 """
 
-from .synth import CONFIGS, Workload, get_config, make_conv_inputs, make_rmsnorm_inputs, make_scan_inputs
+from .synth import (CONFIGS, RMS_EPS, Workload, get_config, make_conv_inputs, make_rmsnorm_inputs, make_scan_inputs,
+                    round_to)
 
-__all__ = ["CONFIGS", "Workload", "get_config", "make_scan_inputs", "make_conv_inputs", "make_rmsnorm_inputs"]
+__all__ = ["CONFIGS", "RMS_EPS", "Workload", "get_config", "make_scan_inputs", "make_conv_inputs",
+           "make_rmsnorm_inputs", "round_to"]
