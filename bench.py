@@ -393,6 +393,24 @@ def main():
             "rmsnorm_fwd": (lambda: lib.rmsnorm_fwd(p(X["r_x"]), p(X["r_scale"]), ctypes.c_float(1e-5), p(N_["r_y"]),
                                                     p(N_["r_rms"]), B * L, H, sdt, sp), B * L * (2 * H * e + 4)),
         }
+        # decode: one token for Bd sequences of this layer; Bd = 1024 puts the state (Bd*D*N fp32) above L2
+        Bd = 1024
+        g = torch.Generator(device=dev).manual_seed(rank)
+        dec = {"x": torch.randn((Bd, D), device=dev, generator=g).to(tdt),
+               "delta": (0.001 + 0.099 * torch.rand((Bd, D), device=dev, generator=g)).to(tdt),
+               "z": torch.randn((Bd, D), device=dev, generator=g).to(tdt),
+               "Bm": torch.randn((Bd, N), device=dev, generator=g).to(tdt),
+               "Cm": torch.randn((Bd, N), device=dev, generator=g).to(tdt),
+               "h": torch.zeros((Bd, D, N), **f32), "y": torch.empty((Bd, D), device=dev, dtype=tdt),
+               "cs": torch.zeros((Bd, D, K), **f32), "co": torch.empty((Bd, D), device=dev, dtype=tdt)}
+        extra["scan_step_decode"] = (
+            lambda: lib.ss_scan_step(p(dec["x"]), p(dec["delta"]), p(X["A"]), p(dec["Bm"]), p(dec["Cm"]), p(X["Dv"]),
+                                     p(dec["z"]), p(dec["h"]), p(dec["y"]), Bd, D, N, sdt, sp),
+            2 * Bd * D * N * 4 + 4 * Bd * D * e + 2 * Bd * N * e + D * N * 4 + D * 4)
+        extra["conv_step_decode"] = (
+            lambda: lib.conv1d_causal_step(p(dec["x"]), p(dec["cs"]), p(X["c_w"]), p(c_bias), p(dec["co"]), Bd, D, K, 1,
+                                           sdt, sp),
+            2 * Bd * D * K * 4 + 2 * Bd * D * e + D * K * 4 + D * 4)
         for n, (fn, nbytes) in extra.items():
             for _ in range(3):
                 if fn() != 0:

@@ -254,6 +254,37 @@ int rmsnorm_fwd(const void* x, const float* scale, float eps, void* y, float* rm
                 int rows, int dim, int dtype, void* stream);
 
 /*
+ * ss_scan_step — one recurrent step of the selective SSM for B independent
+ * sequences (decode): the recurrence of ss_scan_fwd at a single t, with the
+ * state carried in place.  Running it L times from h equals ss_scan_fwd over
+ * those L steps from h0 = h (up to rounding order): the rustytorch
+ * rtx-transformers tests listing (mamba_step_equivalence.rs) exposes the
+ * recurrent state as a single-step updater pinned by that equivalence.
+ *   x, delta, z : [B, D] (dtype);  Bm, Cm : [B, N] (dtype)
+ *   A : [D, N] fp32;  Dv : [D] fp32
+ *   h : [B, D, N] fp32, read and overwritten with the new state
+ *   y : [B, D] (dtype) output: (sum_n Cm[n] h[d,n] + Dv[d] x[d]) * silu(z[d])
+ * N in {4, 8, 16}; A and h 16-byte aligned.
+ */
+int ss_scan_step(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm,
+                 const float* Dv, const void* z, float* h, void* y, int B, int D, int N, int dtype,
+                 void* stream);
+
+/*
+ * conv1d_causal_step — one step of the depthwise causal conv1d (+ optional
+ * SiLU) for B sequences, with the shift register carried in place (mamba-rs
+ * backward_ops.rs, backward_conv1d_step: the current input enters at tap
+ * d_conv-1):
+ *   conv_state : [B, D, d_conv] fp32, newest input at index d_conv-1; every
+ *                tap moves one place towards 0 and x enters at d_conv-1
+ *   out[b,d]   = act(bias[d] + sum_k w[d,k] * conv_state[b,d,k])   (after the shift)
+ *   x, out : [B, D] (dtype);  w : [D, d_conv] fp32;  bias : [D] fp32 or NULL
+ * Running it L times from a zero state equals conv1d_causal_fwd over L steps.
+ */
+int conv1d_causal_step(const void* x, float* conv_state, const float* w, const float* bias, void* out,
+                       int B, int D, int d_conv, int silu, int dtype, void* stream);
+
+/*
  * ss_device_status — synchronises `stream`, then reads and clears the
  * library's device-side error word.  Returns SS_OK, or SS_ERR_DEVICE when a
  * kernel gave up on a bounded wait for its own asynchronous copies since the

@@ -42,6 +42,8 @@ SIGNATURES = {
     "rmsnorm_bwd_noalloc": (_i, [_vp] * 6 + [_i] * 3 + [_vp]),
     "conv1d_causal_fwd": (_i, [_vp] * 4 + [_i] * 6 + [_vp]),
     "rmsnorm_fwd": (_i, [_vp, _vp, ctypes.c_float, _vp, _vp, _i, _i, _i, _vp]),
+    "ss_scan_step": (_i, [_vp] * 9 + [_i] * 4 + [_vp]),
+    "conv1d_causal_step": (_i, [_vp] * 5 + [_i] * 5 + [_vp]),
     "ss_device_status": (_i, [_vp]),
 }
 

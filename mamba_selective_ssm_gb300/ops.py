@@ -12,6 +12,8 @@ Names and argument order follow include/ssscan.h:
 * ``conv1d_causal_fwd(x, w, bias=None, silu=False)`` -> ``out``
 * ``conv1d_causal_silu_bwd(dact, x, w, bias=None, dw=None, db=None)`` -> ``(dx, dw, db)``
 * ``rmsnorm_fwd(x, scale, eps)`` -> ``(y, rms)``
+* ``ss_scan_step(x, delta, A, Bm, Cm, Dv, z, h)`` -> ``y`` (h updated in place)
+* ``conv1d_causal_step(x, conv_state, w, bias=None, silu=False)`` -> ``out`` (state updated in place)
 
 Activations are ``torch.float32`` or ``torch.bfloat16`` CUDA tensors, contiguous;
 parameters, states and gradients are ``torch.float32``.
@@ -234,6 +236,45 @@ def rmsnorm_fwd(x, scale, eps: float, want_rms: bool = True):
     rc = lib.rmsnorm_fwd(_p(x), _p(scale), float(eps), _p(y), _p(rms), R, H, dt, _stream())
     check(rc, "rmsnorm_fwd")
     return y, rms
+
+
+def ss_scan_step(x, delta, A, Bm, Cm, Dv, z, h):
+    """One decode step for B sequences: updates ``h`` [B,D,N] in place and returns y [B,D]."""
+    lib = load()
+    B, D = x.shape
+    N = A.shape[1]
+    dev, dt = x.device, x.dtype
+    _act_dtype(x)
+    for name, t in (("x", x), ("delta", delta), ("z", z)):
+        _req(t, name, (B, D), dt, dev)
+    for name, t in (("Bm", Bm), ("Cm", Cm)):
+        _req(t, name, (B, N), dt, dev)
+    _req(A, "A", (D, N), torch.float32, dev)
+    _req(Dv, "Dv", (D,), torch.float32, dev)
+    _req(h, "h", (B, D, N), torch.float32, dev)
+    y = torch.empty_like(x)
+    rc = lib.ss_scan_step(_p(x), _p(delta), _p(A), _p(Bm), _p(Cm), _p(Dv), _p(z), _p(h), _p(y), B, D, N, _DT[dt],
+                          _stream())
+    check(rc, "ss_scan_step")
+    return y
+
+
+def conv1d_causal_step(x, conv_state, w, bias=None, silu: bool = False):
+    """One conv step for B sequences: shifts ``conv_state`` [B,D,K] in place and returns out [B,D]."""
+    lib = load()
+    B, D = x.shape
+    K = w.shape[1]
+    dev = x.device
+    xdt = _act_dtype(x)
+    _req(conv_state, "conv_state", (B, D, K), torch.float32, dev)
+    _req(w, "w", (D, K), torch.float32, dev)
+    if bias is not None:
+        _req(bias, "bias", (D,), torch.float32, dev)
+    out = torch.empty_like(x)
+    rc = lib.conv1d_causal_step(_p(x), _p(conv_state), _p(w), _p(bias), _p(out), B, D, K, int(bool(silu)), xdt,
+                                _stream())
+    check(rc, "conv1d_causal_step")
+    return out
 
 
 def device_status() -> int:

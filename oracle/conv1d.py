@@ -75,6 +75,18 @@ def conv1d_causal_bwd_ref(dout, x, w):
     return dx, dw, db
 
 
+def conv1d_step_fwd_ref(state, x_t, w, bias=None, silu: bool = False):
+    """One step of the causal conv for B sequences: state [B,D,K] (newest input at
+    K-1) shifts one tap towards 0 and takes x_t [B,D] at K-1; the output is
+    act(bias + sum_k w[:,k] state[..., k]).  Returns (new_state, out)."""
+    state = np.asarray(state, np.float64)
+    new = np.concatenate([state[:, :, 1:], np.asarray(x_t, np.float64)[:, :, None]], axis=2)
+    out = np.sum(new * np.asarray(w, np.float64)[None, :, :], axis=2)
+    if bias is not None:
+        out = out + np.asarray(bias, np.float64)[None, :]
+    return new, (silu_ref(out) if silu else out)
+
+
 def dsilu_ref(v):
     """d/dv silu(v) = s (1 + v (1 - s)), s = 1 / (1 + exp(-v)), float64."""
     v = np.asarray(v, np.float64)

@@ -69,6 +69,18 @@ def scan_fwd_ref(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int | None = None):
     return y, h, ckpt
 
 
+def scan_step_ref(h, x_t, delta_t, A, B_t, C_t, Dv, z_t):
+    """One recurrent step for B sequences (the single-step updater of the
+    rustytorch mamba_step_equivalence.rs test): h [B,D,N], x_t/delta_t/z_t [B,D],
+    B_t/C_t [B,N].  Returns (h_new [B,D,N], y_t [B,D])."""
+    h = np.asarray(h, np.float64)
+    x_t, delta_t, z_t = (np.asarray(v, np.float64) for v in (x_t, delta_t, z_t))
+    A, B_t, C_t, Dv = (np.asarray(v, np.float64) for v in (A, B_t, C_t, Dv))
+    _, h_new = _step(h, delta_t, x_t, B_t, A)
+    s = np.sum(h_new * C_t[:, None, :], axis=-1) + Dv[None, :] * x_t
+    return h_new, s * (z_t * _sigmoid(z_t))
+
+
 def scan_bwd_ref(x, delta, A, Bm, Cm, Dv, z, dy, h0=None, dh_last=None, segment: int | None = None):
     """Reverse-mode gradient of sum(y * dy) + sum(h_last * dh_last) w.r.t. every input of ``scan_fwd_ref``.
 

@@ -142,6 +142,28 @@ def test_layer_fwd_validation(lib):
     assert rms(dt=2) == c.SS_ERR_UNSUPPORTED
 
 
+def test_decode_step_validation(lib):
+    from mamba_selective_ssm_gb300 import _capi as c
+    p = [_fake(0x30000 + 256 * i) for i in range(9)]
+    step = lambda ptrs=p, B=2, D=16, N=16, dt=c.SS_F32: lib.ss_scan_step(*ptrs, B, D, N, dt, None)
+    q = list(p)
+    q[7] = None
+    assert step(q) == c.SS_ERR_NULL
+    assert step(N=5) == c.SS_ERR_UNSUPPORTED
+    assert step(B=0) == c.SS_ERR_DIM
+    assert step(dt=9) == c.SS_ERR_UNSUPPORTED
+    q = list(p)
+    q[7] = _fake(0x30004)  # h
+    assert step(q) == c.SS_ERR_ALIGN
+    r = [_fake(0x40000 + 256 * i) for i in range(5)]
+    conv = lambda ptrs=r, B=2, D=16, K=4, dt=c.SS_BF16: lib.conv1d_causal_step(*ptrs, B, D, K, 1, dt, None)
+    q = list(r)
+    q[1] = None
+    assert conv(q) == c.SS_ERR_NULL
+    assert conv(K=5) == c.SS_ERR_UNSUPPORTED
+    assert conv(D=0) == c.SS_ERR_DIM
+
+
 def test_conv_and_rms_validation(lib):
     from mamba_selective_ssm_gb300 import _capi as c
     assert lib.conv1d_causal_bwd_workspace_size(4, 2048, 4096, 4) > 0

@@ -208,3 +208,17 @@ def test_conv_silu_backward_finite_differences():
             arr[idx] = v0
             fd[idx] = (lp - lm) / 2e-6
         assert max_rel_err(g, fd) < 1e-8
+
+
+@pytest.mark.parametrize("K,silu", [(1, False), (3, True), (4, False), (4, True)])
+def test_conv_step_chain_equals_sequence(K, silu):
+    """L single conv steps from a zero shift register reproduce the full-sequence conv (+SiLU)."""
+    from oracle import conv1d_causal_silu_fwd_ref, conv1d_step_fwd_ref
+    rng = np.random.default_rng(73 + K)
+    x, w, b, _ = _conv_inputs(rng, B=2, L=8, D=3, K=K)
+    ref = (conv1d_causal_silu_fwd_ref if silu else conv1d_causal_fwd_ref)(x, w, b)
+    state = np.zeros((2, 3, K))
+    for t in range(8):
+        state, out = conv1d_step_fwd_ref(state, x[:, t], w, b, silu=silu)
+        np.testing.assert_allclose(out, ref[:, t], rtol=1e-14, atol=1e-14)
+    np.testing.assert_array_equal(state[:, :, -1], x[:, -1])

@@ -284,3 +284,38 @@ def test_bwd_segment_recompute_is_exact():
     g2 = _bwd(p, segment=4)
     for k in g1:
         np.testing.assert_array_equal(g1[k], g2[k])
+
+
+def test_scan_step_chain_equals_sequence():
+    """The single-step updater, called L times with the state carried, is the sequence scan."""
+    from oracle import scan_step_ref
+    rng = np.random.default_rng(21)
+    p = _rand_inputs(rng, B=2, L=9, D=3, N=4)
+    y, h_last, _ = _fwd(p)
+    h = p["h0"]
+    for t in range(9):
+        h, yt = scan_step_ref(h, p["x"][:, t], p["delta"][:, t], p["A"], p["Bm"][:, t], p["Cm"][:, t], p["Dv"],
+                              p["z"][:, t])
+        np.testing.assert_array_equal(yt, y[:, t])
+    np.testing.assert_array_equal(h, h_last)
+
+
+def test_scan_step_scalar_loop():
+    """Brute force: one step written as scalar loops over (b, d, n) with math.exp."""
+    import math
+    from oracle import scan_step_ref
+    rng = np.random.default_rng(22)
+    Bsz, D, N = 2, 3, 4
+    h = rng.standard_normal((Bsz, D, N))
+    x, dt, z = rng.standard_normal((Bsz, D)), rng.uniform(0.01, 0.5, (Bsz, D)), rng.standard_normal((Bsz, D))
+    A, Bt, Ct, Dv = -rng.uniform(0.5, 3, (D, N)), rng.standard_normal((Bsz, N)), rng.standard_normal((Bsz, N)), rng.standard_normal(D)
+    h1, y = scan_step_ref(h, x, dt, A, Bt, Ct, Dv, z)
+    for b in range(Bsz):
+        for d in range(D):
+            s = Dv[d] * x[b, d]
+            for n in range(N):
+                hn = math.exp(dt[b, d] * A[d, n]) * h[b, d, n] + dt[b, d] * Bt[b, n] * x[b, d]
+                assert abs(hn - h1[b, d, n]) <= 1e-13 * (1 + abs(hn))
+                s += Ct[b, n] * hn
+            yv = s * z[b, d] / (1 + math.exp(-z[b, d]))
+            assert abs(yv - y[b, d]) <= 1e-12 * (1 + abs(yv))
