@@ -305,11 +305,11 @@ def main():
     calls = {
         "scan_fwd": lambda: lib.ss_scan_fwd(p(X["x"]), p(X["delta"]), p(X["A"]), p(X["Bm"]), p(X["Cm"]), p(X["Dv"]),
                                             p(X["z"]), None, p(O["y"]), p(O["ckpt"]), p(O["h_last"]),
-                                            B, L, D, N, chunk, sdt, p(W), wsz, sp),
+                                            B, L, D, N, chunk, sdt, None, 0, p(W), wsz, sp),
         "scan_bwd": lambda: lib.ss_scan_bwd(p(X["x"]), p(X["delta"]), p(X["A"]), p(X["Bm"]), p(X["Cm"]), p(X["Dv"]),
                                             p(X["z"]), p(O["ckpt"]), p(X["dy"]), None, p(O["dx"]), p(O["ddelta"]),
                                             p(O["dz"]), p(O["dA"]), p(O["dB"]), p(O["dC"]), p(O["dD"]), p(O["dh0"]),
-                                            B, L, D, N, chunk, sdt, p(W), wsz, sp),
+                                            B, L, D, N, chunk, sdt, None, 0, None, p(W), wsz, sp),
         "conv1d_bwd": lambda: lib.conv1d_causal_bwd(p(X["c_dout"]), p(X["c_x"]), p(X["c_w"]), p(O["c_dx"]),
                                                     p(O["c_dw"]), p(O["c_db"]), B, L, D, K, sdt, p(W), wsz, sp),
         "rmsnorm_bwd": lambda: lib.rmsnorm_bwd(p(X["r_dy"]), p(X["r_x"]), p(X["r_scale"]), p(X["r_rms"]),
@@ -393,6 +393,18 @@ def main():
             "rmsnorm_fwd": (lambda: lib.rmsnorm_fwd(p(X["r_x"]), p(X["r_scale"]), ctypes.c_float(1e-5), p(N_["r_y"]),
                                                     p(N_["r_rms"]), B * L, H, sdt, sp), B * L * (2 * H * e + 4)),
         }
+        # the scan with delta = softplus(raw + dt_bias) computed in its prologues (same tensors, delta read as raw)
+        dtb = torch.zeros((D,), **f32)
+        ddtb = torch.zeros((D,), **f32)
+        extra["scan_fwd_fused_softplus"] = (
+            lambda: lib.ss_scan_fwd(p(X["x"]), p(X["delta"]), p(X["A"]), p(X["Bm"]), p(X["Cm"]), p(X["Dv"]), p(X["z"]),
+                                    None, p(O["y"]), p(O["ckpt"]), p(O["h_last"]), B, L, D, N, chunk, sdt, p(dtb), 1,
+                                    p(W), wsz, sp), alg["scan_fwd"] + D * 4)
+        extra["scan_bwd_fused_softplus"] = (
+            lambda: lib.ss_scan_bwd(p(X["x"]), p(X["delta"]), p(X["A"]), p(X["Bm"]), p(X["Cm"]), p(X["Dv"]), p(X["z"]),
+                                    p(O["ckpt"]), p(X["dy"]), None, p(O["dx"]), p(O["ddelta"]), p(O["dz"]), p(O["dA"]),
+                                    p(O["dB"]), p(O["dC"]), p(O["dD"]), p(O["dh0"]), B, L, D, N, chunk, sdt, p(dtb), 1,
+                                    p(ddtb), p(W), wsz, sp), alg["scan_bwd"] + 2 * D * 4)
         # decode: one token for Bd sequences of this layer; Bd = 1024 puts the state (Bd*D*N fp32) above L2
         Bd = 1024
         g = torch.Generator(device=dev).manual_seed(rank)

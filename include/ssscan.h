@@ -89,6 +89,12 @@ size_t ss_scan_fwd_workspace_size(int B, int L, int D, int N, int chunk, int dty
  *                 lets the backward skip its recompute pass at the price of
  *                 N*4 bytes of checkpoint per 8 steps and channel.
  *   N           : 4, 8 or 16;  D: a multiple of 8
+ *   dt_bias, delta_softplus : the discretisation of delta fused in front of
+ *                 the scan (the Mamba layer's delta = softplus(raw + dt_bias)):
+ *                 the recurrence uses f(delta + dt_bias[d]) with f = softplus
+ *                 when delta_softplus != 0 (softplus(v) = log(1 + e^v)), else
+ *                 the identity; dt_bias is [D] fp32 or NULL (zero).  With
+ *                 dt_bias NULL and delta_softplus 0, delta is used as given.
  *   workspace   : device scratch of at least ss_scan_fwd_workspace_size()
  *                 bytes (NULL allowed when that is 0), 16-byte aligned,
  *                 contents need not be initialised.  When B*D is small the
@@ -101,6 +107,7 @@ int ss_scan_fwd(const void* x, const void* delta, const float* A, const void* Bm
                 const float* Dv, const void* z, const float* h0,
                 void* y, float* ckpt, float* h_last,
                 int B, int L, int D, int N, int chunk, int dtype,
+                const float* dt_bias, int delta_softplus,
                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
@@ -127,6 +134,11 @@ size_t ss_scan_bwd_workspace_size(int B, int L, int D, int N, int chunk, int dty
  *   dx_t = ds_t*D + delta_t*sum_n G_t*B_t;  dz_t = dy_t*s_t*silu'(z_t);
  *   dA += sum q_t*delta_t;  dB_t = sum_d G_t*delta_t*x_t;  dC_t = sum_d ds_t*h_t;
  *   dD += sum ds_t*x_t;  dh0 = a_0*G_0.
+ * With the fused discretisation (dt_bias / delta_softplus as in ss_scan_fwd,
+ * which must have been called with the same values), ddelta is the gradient
+ * with respect to the raw delta: the above times softplus'(v) = sigmoid(v)
+ * (evaluated as 1 - exp(-delta)) when delta_softplus, and
+ *   d_dt_bias : [D] fp32, accumulated (+=) with sum_{b,t} of that ddelta, or NULL.
  * The states are rebuilt chunk by chunk from `ckpt`, never stored in full.
  * workspace: device scratch of at least ss_scan_bwd_workspace_size() bytes,
  *   16-byte aligned, contents need not be initialised.
@@ -135,6 +147,7 @@ int ss_scan_bwd(const void* x, const void* delta, const float* A, const void* Bm
                 const float* Dv, const void* z, const float* ckpt, const void* dy, const float* dh_last,
                 float* dx, float* ddelta, float* dz, float* dA, float* dB, float* dC, float* dD, float* dh0,
                 int B, int L, int D, int N, int chunk, int dtype,
+                const float* dt_bias, int delta_softplus, float* d_dt_bias,
                 void* workspace, size_t ws_bytes, void* stream);
 
 /*

@@ -61,9 +61,14 @@ struct BwdSmem {
   // the lane's 2 channels (row pitch CG*N + 16 keeps the epilogue's 128-bit reads conflict-free)
   alignas(16) float dbc[W][kS][2][CG * N + 16];
   alignas(16) float Dv_s[DT];
+  alignas(16) float bias_s[DT];  // dt_bias of the fused discretisation (0 without one)
   alignas(8) uint64_t full[NSTG];
   uint32_t tmem_base;
 };
+
+// Four 32-channel bf16 CTAs (N = 16, the register-limited residency) must also
+// fit the SM's 228 KB of shared memory, 1 KB of which each CTA reserves.
+static_assert(sizeof(BwdSmem<__nv_bfloat16, 16, 2, 32>) + 1024 <= 228 * 1024 / 4, "four backward CTAs per SM");
 
 // TMEM columns: 8 per window boundary of a chunk, rounded up to a power of two >= 32
 inline uint32_t tmem_cols(int chunk) {
@@ -83,12 +88,16 @@ struct BwdParams {
   float* dz;
   float* dh0;
   float* ws_dBC;  // [channel tiles][B][L][2N]
-  float* ws_dAD;  // [CTA rows][D*N + D]: dA then dD partials of each CTA row
+  float* ws_dAD;  // [CTA rows][D*N + 2D]: dA, dD and d dt_bias partials of each CTA row
   int B, L, D, chunk, nchunks;
   uint32_t tcols;
   int P, Ls;      // sequence segments (P = 1: one CTA row walks whole batch rows)
   float* gsum;    // [B][P][D][N] adjoint a_tb G_tb at each segment's start from a zero carry at its end
   float* dsum;    // [B][P][D]    sum of delta over each segment
+  const float* dt_bias;  // fused discretisation: delta = f(raw + dt_bias), f = softplus if dsp
+  int dsp;
+  int fuse;              // dt_bias != NULL or dsp
+  float* d_dt_bias;      // [D] accumulated gradient of dt_bias, or NULL
 };
 
 template <typename T, int N, int NSTG, int DT>
@@ -100,13 +109,14 @@ struct BwdSumSmem {
   alignas(16) float dlt_f[kTT * DT];
   alignas(16) float ds_f[kTT * DT];
   alignas(16) float C_f[kTT * N];
+  alignas(16) float bias_s[DT];
   alignas(8) uint64_t full[NSTG];
 };
 
 // Segment summaries for segments 1 .. P-1: the adjoint each carries out of its
 // first step when the carry entering its last step is zero, and its sum of
 // delta.  CTA = (channel tile, (batch row, segment)); tiles walked last to first.
-template <int N, typename T, int NSTG, int DT>
+template <int N, typename T, int NSTG, int DT, bool FUSE>
 __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const BwdParams p,
                                                                        const __grid_constant__ CUtensorMap tm_dlt,
                                                                        const __grid_constant__ CUtensorMap tm_z,
@@ -145,6 +155,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
     tma_load_3d(S.dy[slot], &tm_dy, &S.full[slot], d0, t0, b);
     tma_load_2d(S.Cm[slot], &tm_C, &S.full[slot], t0 * N, b);
   };
+  for (int c = tid; c < DT; c += G::NT) S.bias_s[c] = (p.dt_bias != nullptr && d0 + c < p.D) ? p.dt_bias[d0 + c] : 0.f;
   if (tid == 0) {
     prefetch_tmap(&tm_dlt); prefetch_tmap(&tm_z); prefetch_tmap(&tm_dy); prefetch_tmap(&tm_C);
     for (int st = 0; st < NSTG; ++st) mbar_init(&S.full[st], 1);
@@ -173,6 +184,10 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
       AT::ld4(&S.dlt[slot][gi * 4], dv);
       AT::ld4(&S.z[slot][gi * 4], zv);
       AT::ld4(&S.dy[slot][gi * 4], gv);
+      if constexpr (FUSE) {
+        const int c4 = (gi % (DT / 4)) * 4;
+        delta_transform4(dv, S.bias_s, c4, (gte - 1 - k) * kTT + gi / (DT / 4) < p.L, p.D - d0 - c4, p.dsp);
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) gv[e] *= zv[e] * sigmoid(zv[e]);
       reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
@@ -212,7 +227,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
   }
 }
 
-template <int N, typename T, int NSTG, int DT>
+template <int N, typename T, int NSTG, int DT, bool FUSE>
 __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
                                                               const __grid_constant__ CUtensorMap tm_x,
                                                               const __grid_constant__ CUtensorMap tm_z,
@@ -262,7 +277,10 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
         Ap[j][q] = f2(0.f, 0.f);
       }
     }
-  for (int c = tid; c < DT; c += G::NT) S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
+  for (int c = tid; c < DT; c += G::NT) {
+    S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
+    S.bias_s[c] = (p.dt_bias != nullptr && d0 + c < p.D) ? p.dt_bias[d0 + c] : 0.f;
+  }
 
   // Items of a batch row, in order.  Direct mode: tiles gte-1 down to gtb.
   // Otherwise per chunk kc = ce-1 down to tb/chunk: pass A over its ntc tiles
@@ -351,10 +369,11 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
   float2 ga[2][2];             // a_{t+1} * G_{t+1}: the adjoint carried backwards
   float2 dA2[2][2];            // dA partial sums of the thread's cells
   float dDacc[4];              // dD partial sums of the epilogue's four channels
+  float dTacc[4];              // d dt_bias partial sums of the same channels
 #pragma unroll
   for (int j = 0; j < 2; ++j) dA2[j][0] = dA2[j][1] = f2(0.f, 0.f);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) dDacc[e] = 0.f;
+  for (int e = 0; e < 4; ++e) dDacc[e] = dTacc[e] = 0.f;
   bool failed = false;
 
   Cursor cur;
@@ -417,6 +436,10 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
         float dv[4], xv[4];
         AT::ld4(&S.dlt[slot][gi * 4], dv);
         AT::ld4(&S.x[slot][gi * 4], xv);
+        if constexpr (FUSE) {
+          const int c4 = (gi % (DT / 4)) * 4;
+          delta_transform4(dv, S.bias_s, c4, t0 + gi / (DT / 4) < L, p.D - d0 - c4, p.dsp);
+        }
         reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
         reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(dv[0] * xv[0], dv[1] * xv[1], dv[2] * xv[2], dv[3] * xv[3]);
       }
@@ -483,6 +506,10 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
       AT::ld4(&S.x[slot][gi * 4], xv);
       AT::ld4(&S.z[slot][gi * 4], zv);
       AT::ld4(&S.dy[slot][gi * 4], gv);
+      if constexpr (FUSE) {
+        const int c4 = (gi % (DT / 4)) * 4;
+        delta_transform4(dv, S.bias_s, c4, t0 + gi / (DT / 4) < L, p.D - d0 - c4, p.dsp);
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float sg = sigmoid(zv[e]);
@@ -671,6 +698,13 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
             o2[e] = gz[e] * s;                             // dz
             dDacc[e] = fmaf(dsa[e], xv[e], dDacc[e]);
           }
+          if constexpr (FUSE) {  // back through delta = softplus(v): softplus'(v) = sigmoid(v) = 1 - exp(-delta)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (p.dsp) o1[e] *= softplus_grad_from_delta(dv[e]);
+              dTacc[e] += o1[e];
+            }
+          }
           const size_t off = ((size_t)b * L + t) * p.D + d;
           *reinterpret_cast<float4*>(p.dx + off) = make_float4(o0[0], o0[1], o0[2], o0[3]);
           *reinterpret_cast<float4*>(p.ddelta + off) = make_float4(o1[0], o1[1], o1[2], o1[3]);
@@ -696,23 +730,29 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
   if (warp == 0 && !direct) tmem_dealloc(S.tmem_base, p.tcols);
   if (failed) return;
 
-  // per-CTA partials of dA and dD (summed over this CTA's batch rows)
+  // per-CTA partials of dA, dD and d dt_bias (summed over this CTA's batch rows)
+  float* row = p.ws_dAD + (size_t)blockIdx.y * p.D * (N + 2);
   if (dvalid) {
 #pragma unroll
     for (int j = 0; j < 2; ++j)
-      *reinterpret_cast<float4*>(p.ws_dAD + (size_t)blockIdx.y * p.D * (N + 1) + (size_t)(dg + j) * N + n0) =
+      *reinterpret_cast<float4*>(row + (size_t)(dg + j) * N + n0) =
           make_float4(dA2[j][0].x, dA2[j][0].y, dA2[j][1].x, dA2[j][1].y);
   }
-  // dD: threads with equal tid % 16 hold the same four channels
+  // dD, d dt_bias: threads with equal tid % (DT/4) hold the same four channels
   float* red = &S.sab[0][0][0];  // free after the last window
   *reinterpret_cast<float4*>(&red[tid * 4]) = make_float4(dDacc[0], dDacc[1], dDacc[2], dDacc[3]);
+  *reinterpret_cast<float4*>(&red[(G::NT + tid) * 4]) = make_float4(dTacc[0], dTacc[1], dTacc[2], dTacc[3]);
   __syncthreads();
   for (int c = tid; c < DT; c += G::NT) {
     if (d0 + c < p.D) {
       const int grp = c / 4, e = c % 4;
-      float acc = 0.f;
-      for (int m = grp; m < G::NT; m += DT / 4) acc += red[m * 4 + e];
-      p.ws_dAD[(size_t)blockIdx.y * p.D * (N + 1) + (size_t)p.D * N + d0 + c] = acc;
+      float accD = 0.f, accT = 0.f;
+      for (int m = grp; m < G::NT; m += DT / 4) {
+        accD += red[m * 4 + e];
+        accT += red[(G::NT + m) * 4 + e];
+      }
+      row[(size_t)p.D * N + d0 + c] = accD;
+      row[(size_t)p.D * (N + 1) + d0 + c] = accT;
     }
   }
 }
@@ -730,14 +770,17 @@ __global__ void ss_bwd_dbc_kernel(const float* __restrict__ ws_dBC, float* dB, f
   }
 }
 
-// dA (first D*N columns of a partial row) and dD (last D columns) accumulate.
+// dA (first D*N columns of a partial row), dD (next D) and d dt_bias (last D,
+// when asked for) accumulate.
 struct DADStore {
   float* dA;
   float* dD;
-  long long nA;
+  float* dT;
+  long long nA, D;
   __device__ void put(long long i, float v) const {
     if (i < nA) dA[i] += v;
-    else dD[i - nA] += v;
+    else if (i < nA + D) dD[i - nA] += v;
+    else if (dT != nullptr) dT[i - nA - D] += v;
   }
 };
 
@@ -766,7 +809,7 @@ inline BwdPlan make_plan(int B, int L, int D, int N, int chunk) {
   const int rows = pl.pmax > 1 && B * pl.pmax > pl.gy ? B * pl.pmax : pl.gy;
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
   pl.off_dAD = up((size_t)pl.ndt * B * L * 2 * N * sizeof(float));
-  pl.off_gsum = up(pl.off_dAD + (size_t)rows * D * (N + 1) * sizeof(float));
+  pl.off_gsum = up(pl.off_dAD + (size_t)rows * D * (N + 2) * sizeof(float));
   pl.off_dsum = up(pl.off_gsum + (pl.pmax > 1 ? (size_t)B * pl.pmax * D * N * sizeof(float) : 0));
   pl.total = pl.off_dsum + (pl.pmax > 1 ? (size_t)B * pl.pmax * D * sizeof(float) : 0);
   return pl;
@@ -779,9 +822,9 @@ struct Stages {
   static constexpr int value = 2;
 };
 
-template <int N, typename T, int NSTG = Stages<T>::value, int DT = bwd_dt<N>()>
-int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, const void* dy,
-               float* dA, float* dB, float* dC, float* dD, void* ws, cudaStream_t stream) {
+template <int N, typename T, int NSTG, int DT, bool FUSE>
+int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, const void* dy,
+                 float* dA, float* dB, float* dC, float* dD, void* ws, cudaStream_t stream) {
   constexpr int e = ActT<T>::kBytes;
   const BwdPlan pl = make_plan(p.B, p.L, p.D, N, p.chunk);
   p.ws_dBC = static_cast<float*>(ws);
@@ -804,7 +847,7 @@ int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, co
       !ssh::encode_tiled(&tm[5], ActT<T>::kTma, 2, Cm, bdims, bstr, bbox))
     return SS_ERR_CUDA;
   const size_t smem = sizeof(BwdSmem<T, N, NSTG, DT>);
-  auto kern = scan_bwd_kernel<N, T, NSTG, DT>;
+  auto kern = scan_bwd_kernel<N, T, NSTG, DT, FUSE>;
   // TMEM: the CTAs resident on one SM must fit in its 512 columns, else an
   // allocation would wait for another CTA to finish.  Ask for enough shared
   // memory per CTA to keep the residency within that bound.
@@ -838,7 +881,7 @@ int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, co
   if (p.P > 1) {
     rows = p.B * p.P;
     const size_t smem_s = sizeof(BwdSumSmem<T, N, NSTG, DT>);
-    auto skern = scan_bwd_summary_kernel<N, T, NSTG, DT>;
+    auto skern = scan_bwd_summary_kernel<N, T, NSTG, DT, FUSE>;
     if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s) != cudaSuccess)
       return SS_ERR_CUDA;
     skern<<<dim3(pl.ndt, p.B * (p.P - 1)), Geo<N, DT>::NT, smem_s, stream>>>(p, tm[0], tm[2], tm[3], tm[5]);
@@ -852,7 +895,16 @@ int launch_bwd(BwdParams p, const void* x, const void* delta, const void* Bm, co
   ss_bwd_dbc_kernel<N><<<(int)blocks, 256, 0, stream>>>(p.ws_dBC, dB, dC, nBC, pl.ndt);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
   const long long nA = (long long)p.D * N;
-  return colsum(p.ws_dAD, nA + p.D, rows, DADStore{dA, dD, nA}, stream) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  return colsum(p.ws_dAD, nA + 2ll * p.D, rows, DADStore{dA, dD, p.d_dt_bias, nA, p.D}, stream) == cudaSuccess ? SS_OK
+                                                                                                      : SS_ERR_CUDA;
+}
+
+// the discretisation of delta is a template switch, so the plain scan carries none of it
+template <int N, typename T, int NSTG = Stages<T>::value, int DT = bwd_dt<N>()>
+int launch_bwd(const BwdParams& p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z,
+               const void* dy, float* dA, float* dB, float* dC, float* dD, void* ws, cudaStream_t stream) {
+  return p.fuse ? launch_bwd_f<N, T, NSTG, DT, true>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, ws, stream)
+                : launch_bwd_f<N, T, NSTG, DT, false>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, ws, stream);
 }
 
 int validate_bwd(int B, int L, int D, int N, int chunk, int dtype) {
@@ -885,7 +937,8 @@ extern "C" size_t ss_scan_bwd_workspace_size(int B, int L, int D, int N, int chu
 extern "C" int ss_scan_bwd(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm, const float* Dv,
                            const void* z, const float* ckpt, const void* dy, const float* dh_last, float* dx, float* ddelta,
                            float* dz, float* dA, float* dB, float* dC, float* dD, float* dh0, int B, int L, int D, int N,
-                           int chunk, int dtype, void* workspace, size_t ws_bytes, void* stream) {
+                           int chunk, int dtype, const float* dt_bias, int delta_softplus, float* d_dt_bias,
+                           void* workspace, size_t ws_bytes, void* stream) {
   if (!x || !delta || !A || !Bm || !Cm || !Dv || !z || !ckpt || !dy || !dx || !ddelta || !dz || !dA || !dB || !dC || !dD)
     return SS_ERR_NULL;
   const int v = validate_bwd(B, L, D, N, chunk, dtype);
@@ -898,7 +951,8 @@ extern "C" int ss_scan_bwd(const void* x, const void* delta, const float* A, con
   if (workspace == nullptr || ws_bytes < pl.total) return SS_ERR_WORKSPACE;
   if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
   BwdParams p{A, Dv, ckpt, dh_last, dx, ddelta, dz, dh0, nullptr, nullptr, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 0,
-              1, L, nullptr, nullptr};
+              1, L, nullptr, nullptr, dt_bias, delta_softplus ? 1 : 0, (dt_bias != nullptr || delta_softplus) ? 1 : 0,
+              d_dt_bias};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool wide = bwd_channels(N, chunk) == 64;
   if (dtype == SS_F32) {

@@ -64,6 +64,37 @@ inline SegPlan seg_plan(int p_want, int L, int unit) {
   return SegPlan{(L + Ls - 1) / Ls, Ls};
 }
 
+// ---------------------------------------------------------------- fused discretisation
+// log(1 + u) for u in [0, 1]: the Taylor series u - u^2/2 + u^3/3 below 1/32
+// (truncation below u^4/4, i.e. 7e-6 relative), the fast logarithm of 1 + u
+// above (where 1 + u keeps u to 2e-6 relative).
+__device__ __forceinline__ float log1p_unit(float u) {
+  return u < 0.03125f ? u * fmaf(u, fmaf(u, 1.0f / 3.0f, -0.5f), 1.0f) : __logf(1.0f + u);
+}
+
+// softplus(v) = log(1 + e^v) = max(v, 0) + log(1 + e^-|v|).
+__device__ __forceinline__ float softplus_f(float v) { return fmaxf(v, 0.f) + log1p_unit(__expf(-fabsf(v))); }
+
+// softplus'(v) = sigmoid(v) = 1 - e^-softplus(v), from delta = softplus(v):
+// the series delta - delta^2/2 + delta^3/6 below 1/32 (no cancellation), else 1 - e^-delta.
+__device__ __forceinline__ float softplus_grad_from_delta(float dl) {
+  return dl < 0.03125f ? dl * fmaf(dl, fmaf(dl, 1.0f / 6.0f, -0.5f), 1.0f) : 1.0f - __expf(-dl);
+}
+
+// The delta the recurrence uses, from the caller's raw values: raw + bias, and
+// softplus of that when asked.  Steps past L and channels past D are forced to
+// 0 so that they leave the state unchanged, as the zero-filled raw delta does
+// without the transform.
+__device__ __forceinline__ void delta_transform4(float* dv, const float* bias_s, int c4, bool row_ok, int d_left,
+                                                 int softplus) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float v = dv[e] + bias_s[c4 + e];
+    if (softplus) v = softplus_f(v);
+    dv[e] = (row_ok && e < d_left) ? v : 0.f;
+  }
+}
+
 inline int device_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

@@ -52,6 +52,7 @@ struct FwdSmem {
   alignas(16) float C_f[kTT * N];
   alignas(16) float yp[kTT][N / 4][DT + 8];  // per-lane shares of C_t . h_t over the lane's 4 states (row pitch spreads banks)
   alignas(16) float Dv_s[DT];
+  alignas(16) float bias_s[DT];  // dt_bias of the fused discretisation (0 without one)
   alignas(8) uint64_t full[kNST];
 };
 
@@ -66,6 +67,9 @@ struct FwdParams {
   int P, Ls;     // sequence segments (P = 1: one CTA row walks whole batch rows)
   float* hsum;   // [B][P][D][N] state at the end of each segment from a zero start
   float* dsum;   // [B][P][D]    sum of delta over each segment
+  const float* dt_bias;  // fused discretisation: delta = f(raw + dt_bias), f = softplus if dsp
+  int dsp;
+  int fuse;              // dt_bias != NULL or dsp
 };
 
 template <typename T, int N, int DT>
@@ -76,12 +80,13 @@ struct FwdSumSmem {
   alignas(16) float dlt_f[kTT * DT];
   alignas(16) float dx_f[kTT * DT];
   alignas(16) float B_f[kTT * N];
+  alignas(16) float bias_s[DT];
   alignas(8) uint64_t full[kNST];
 };
 
 // Segment summaries for segments 0 .. P-2: the state each reaches from a zero
 // start, and its sum of delta.  CTA = (channel tile, (batch row, segment)).
-template <int N, typename T, int CPT, int DT>
+template <int N, typename T, int CPT, int DT, bool FUSE>
 __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_summary_kernel(const FwdParams p,
                                                                       const __grid_constant__ CUtensorMap tm_dlt,
                                                                       const __grid_constant__ CUtensorMap tm_x,
@@ -117,6 +122,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_summary_kernel(
     tma_load_3d(S.x[slot], &tm_x, &S.full[slot], d0, t0, b);
     tma_load_2d(S.Bm[slot], &tm_B, &S.full[slot], t0 * N, b);
   };
+  for (int c = tid; c < DT; c += G::NT) S.bias_s[c] = (p.dt_bias != nullptr && d0 + c < p.D) ? p.dt_bias[d0 + c] : 0.f;
   if (tid == 0) {
     prefetch_tmap(&tm_dlt); prefetch_tmap(&tm_x); prefetch_tmap(&tm_B);
     for (int st = 0; st < kNST; ++st) mbar_init(&S.full[st], 1);
@@ -147,6 +153,10 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_summary_kernel(
       float dv[4], xv[4];
       AT::ld4(&S.dlt[slot][gi * 4], dv);
       AT::ld4(&S.x[slot][gi * 4], xv);
+      if constexpr (FUSE) {
+        const int c4 = (gi % (DT / 4)) * 4;
+        delta_transform4(dv, S.bias_s, c4, tb + k * kTT + gi / (DT / 4) < p.L, p.D - d0 - c4, p.dsp);
+      }
       reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
       reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(dv[0] * xv[0], dv[1] * xv[1], dv[2] * xv[2], dv[3] * xv[3]);
     }
@@ -182,7 +192,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_summary_kernel(
   }
 }
 
-template <int N, typename T, int CPT, int DT>
+template <int N, typename T, int CPT, int DT, bool FUSE>
 __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
                                                               const __grid_constant__ CUtensorMap tm_x,
                                                               const __grid_constant__ CUtensorMap tm_z,
@@ -240,7 +250,10 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
         Ap[j][q] = f2(0.f, 0.f);
       }
     }
-  for (int c = tid; c < DT; c += G::NT) S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
+  for (int c = tid; c < DT; c += G::NT) {
+    S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
+    S.bias_s[c] = (p.dt_bias != nullptr && d0 + c < p.D) ? p.dt_bias[d0 + c] : 0.f;
+  }
 
   auto issue = [&](int k) {  // k: the item icur points at
     const int slot = k % kNST;
@@ -310,6 +323,10 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
       float dv[4], xv[4];
       AT::ld4(&S.dlt[slot][gi * 4], dv);
       AT::ld4(&S.x[slot][gi * 4], xv);
+      if constexpr (FUSE) {
+        const int c4 = (gi % (DT / 4)) * 4;
+        delta_transform4(dv, S.bias_s, c4, t0 + gi / (DT / 4) < L, p.D - d0 - c4, p.dsp);
+      }
       reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
       reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(dv[0] * xv[0], dv[1] * xv[1], dv[2] * xv[2], dv[3] * xv[3]);
     }
@@ -423,7 +440,7 @@ size_t fwd_ws_bytes(int B, int L, int D, int N) {
   return (((size_t)B * pm * D * N * sizeof(float) + 255) & ~(size_t)255) + (size_t)B * pm * D * sizeof(float);
 }
 
-template <int N, typename T, int CPT = 1, int DT = kFDT>
+template <int N, typename T, bool FUSE, int CPT = 1, int DT = kFDT>
 int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, void* ws,
                cudaStream_t stream) {
   constexpr int e = ActT<T>::kBytes;
@@ -442,7 +459,7 @@ int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, co
     return SS_ERR_CUDA;
   const int ndt = (p.D + DT - 1) / DT;
   const size_t smem = sizeof(FwdSmem<T, N, DT>);
-  auto kern = scan_fwd_kernel<N, T, CPT, DT>;
+  auto kern = scan_fwd_kernel<N, T, CPT, DT, FUSE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
   // segments: only when (batch row, channel tile) pairs leave SMs idle
   p.P = 1;
@@ -463,7 +480,7 @@ int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, co
   }
   if (p.P > 1) {
     const size_t smem_s = sizeof(FwdSumSmem<T, N, DT>);
-    auto skern = scan_fwd_summary_kernel<N, T, CPT, DT>;
+    auto skern = scan_fwd_summary_kernel<N, T, CPT, DT, FUSE>;
     if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s) != cudaSuccess)
       return SS_ERR_CUDA;
     skern<<<dim3(ndt, p.B * (p.P - 1)), GeoF<N, CPT, DT>::NT, smem_s, stream>>>(p, tm[0], tm[1], tm[3]);
@@ -487,6 +504,15 @@ int read_clear_fwd_err(cudaStream_t s, unsigned* out) {
   return cudaStreamSynchronize(s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 }  // namespace ssh
+
+namespace {
+// the discretisation of delta is a template switch, so the plain scan carries none of it
+template <int N, typename T>
+int fwd_fuse(const FwdParams& p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, void* ws,
+             cudaStream_t s) {
+  return p.fuse ? launch_fwd<N, T, true>(p, x, delta, Bm, Cm, z, ws, s) : launch_fwd<N, T, false>(p, x, delta, Bm, Cm, z, ws, s);
+}
+}  // namespace
 
 extern "C" int ss_scan_num_chunks(int L, int chunk) { return (L > 0 && chunk > 0) ? (L + chunk - 1) / chunk : 0; }
 
@@ -513,7 +539,8 @@ extern "C" size_t ss_scan_fwd_workspace_size(int B, int L, int D, int N, int chu
 
 extern "C" int ss_scan_fwd(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm, const float* Dv,
                            const void* z, const float* h0, void* y, float* ckpt, float* h_last, int B, int L, int D, int N,
-                           int chunk, int dtype, void* workspace, size_t ws_bytes, void* stream) {
+                           int chunk, int dtype, const float* dt_bias, int delta_softplus, void* workspace,
+                           size_t ws_bytes, void* stream) {
   if (!x || !delta || !A || !Bm || !Cm || !Dv || !z || !y || !ckpt) return SS_ERR_NULL;
   const int v = validate_fwd(B, L, D, N, chunk, dtype);
   if (v != SS_OK) return v;
@@ -524,14 +551,15 @@ extern "C" int ss_scan_fwd(const void* x, const void* delta, const float* A, con
   const size_t need = fwd_ws_bytes(B, L, D, N);
   if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SS_ERR_WORKSPACE;
   if (workspace != nullptr && !ssh::aligned16(workspace)) return SS_ERR_ALIGN;
-  FwdParams p{A, Dv, h0, y, ckpt, h_last, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 1, L, nullptr, nullptr};
+  FwdParams p{A, Dv, h0, y, ckpt, h_last, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 1, L, nullptr, nullptr,
+              dt_bias, delta_softplus ? 1 : 0, (dt_bias != nullptr || delta_softplus) ? 1 : 0};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SS_F32) {
-    if (N == 4) return launch_fwd<4, float>(p, x, delta, Bm, Cm, z, workspace, s);
-    if (N == 8) return launch_fwd<8, float>(p, x, delta, Bm, Cm, z, workspace, s);
-    return launch_fwd<16, float>(p, x, delta, Bm, Cm, z, workspace, s);
+    if (N == 4) return fwd_fuse<4, float>(p, x, delta, Bm, Cm, z, workspace, s);
+    if (N == 8) return fwd_fuse<8, float>(p, x, delta, Bm, Cm, z, workspace, s);
+    return fwd_fuse<16, float>(p, x, delta, Bm, Cm, z, workspace, s);
   }
-  if (N == 4) return launch_fwd<4, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
-  if (N == 8) return launch_fwd<8, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
-  return launch_fwd<16, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
+  if (N == 4) return fwd_fuse<4, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
+  if (N == 8) return fwd_fuse<8, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
+  return fwd_fuse<16, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
 }

@@ -69,7 +69,10 @@ def scan_fwd_workspace_size(B, L, D, N, chunk, dtype) -> int:
     return load().ss_scan_fwd_workspace_size(B, L, D, N, chunk, _DT[dtype])
 
 
-def ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int = 64, want_h_last: bool = True, workspace=None):
+def ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int = 64, want_h_last: bool = True, workspace=None,
+                dt_bias=None, delta_softplus: bool = False):
+    """Forward scan -> ``(y, ckpt, h_last)``.  With ``dt_bias`` / ``delta_softplus`` the
+    recurrence uses softplus(delta + dt_bias) (or delta + dt_bias), computed in the kernel."""
     lib = load()
     B, L, D = x.shape
     N = A.shape[1]
@@ -83,6 +86,8 @@ def ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int = 64, want_h_las
     _req(Dv, "Dv", (D,), torch.float32, dev)
     if h0 is not None:
         _req(h0, "h0", (B, D, N), torch.float32, dev)
+    if dt_bias is not None:
+        _req(dt_bias, "dt_bias", (D,), torch.float32, dev)
     nck = num_chunks(L, chunk) if L > 0 and chunk > 0 else 0
     y = torch.empty_like(x)
     ckpt = torch.empty((B, max(nck, 1), D, N), device=dev, dtype=torch.float32)
@@ -92,7 +97,8 @@ def ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int = 64, want_h_las
         workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
     ws_have = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.ss_scan_fwd(_p(x), _p(delta), _p(A), _p(Bm), _p(Cm), _p(Dv), _p(z), _p(h0), _p(y), _p(ckpt), _p(h_last),
-                         B, L, D, N, chunk, _DT[dt], _p(workspace), ws_have, _stream())
+                         B, L, D, N, chunk, _DT[dt], _p(dt_bias), int(bool(delta_softplus)), _p(workspace), ws_have,
+                         _stream())
     check(rc, "ss_scan_fwd")
     return y, ckpt, h_last
 
@@ -102,9 +108,12 @@ def scan_bwd_workspace_size(B, L, D, N, chunk, dtype) -> int:
 
 
 def ss_scan_bwd(x, delta, A, Bm, Cm, Dv, z, ckpt, dy, dh_last=None, chunk: int = 64, dA=None, dD=None,
-                want_dh0: bool = True, workspace=None, out=None):
+                want_dh0: bool = True, workspace=None, out=None, dt_bias=None, delta_softplus: bool = False,
+                d_dt_bias=None):
     """Gradients of sum(y*dy) (+ sum(h_last*dh_last)).  dA and dD accumulate into the
-    given tensors (zeros when None); the rest are returned freshly (or written into ``out``)."""
+    given tensors (zeros when None); the rest are returned freshly (or written into ``out``).
+    With the fused discretisation (same ``dt_bias`` / ``delta_softplus`` as the forward),
+    ``ddelta`` is the gradient of the raw delta and ``d_dt_bias`` accumulates (zeros when None)."""
     lib = load()
     B, L, D = x.shape
     N = A.shape[1]
@@ -127,6 +136,12 @@ def ss_scan_bwd(x, delta, A, Bm, Cm, Dv, z, ckpt, dy, dh_last=None, chunk: int =
             "dC": torch.empty((B, L, N), **f32),
             "dh0": torch.empty((B, D, N), **f32) if want_dh0 else None,
         }
+    fused = dt_bias is not None or delta_softplus
+    if dt_bias is not None:
+        _req(dt_bias, "dt_bias", (D,), torch.float32, dev)
+    if fused:
+        out["d_dt_bias"] = (torch.zeros((D,), **f32) if d_dt_bias is None
+                            else _req(d_dt_bias, "d_dt_bias", (D,), torch.float32, dev))
     out["dA"] = torch.zeros((D, N), **f32) if dA is None else _req(dA, "dA", (D, N), torch.float32, dev)
     out["dD"] = torch.zeros((D,), **f32) if dD is None else _req(dD, "dD", (D,), torch.float32, dev)
     ws_bytes = lib.ss_scan_bwd_workspace_size(B, L, D, N, chunk, _DT[dt])
@@ -134,7 +149,8 @@ def ss_scan_bwd(x, delta, A, Bm, Cm, Dv, z, ckpt, dy, dh_last=None, chunk: int =
         workspace = torch.empty(max(ws_bytes, 16), device=dev, dtype=torch.uint8)
     rc = lib.ss_scan_bwd(_p(x), _p(delta), _p(A), _p(Bm), _p(Cm), _p(Dv), _p(z), _p(ckpt), _p(dy), _p(dh_last),
                          _p(out["dx"]), _p(out["ddelta"]), _p(out["dz"]), _p(out["dA"]), _p(out["dB"]), _p(out["dC"]),
-                         _p(out["dD"]), _p(out.get("dh0")), B, L, D, N, chunk, _DT[dt], _p(workspace),
+                         _p(out["dD"]), _p(out.get("dh0")), B, L, D, N, chunk, _DT[dt], _p(dt_bias),
+                         int(bool(delta_softplus)), _p(out.get("d_dt_bias")), _p(workspace),
                          workspace.numel() * workspace.element_size(), _stream())
     check(rc, "ss_scan_bwd")
     return out

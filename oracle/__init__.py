@@ -31,10 +31,12 @@ and RMSNorm scale invariance.
 from .conv1d import (conv1d_causal_bwd_ref, conv1d_causal_fwd_ref, conv1d_causal_silu_bwd_ref,
                      conv1d_causal_silu_fwd_ref, conv1d_step_bwd_ref, conv1d_step_fwd_ref, dsilu_ref, silu_ref)
 from .rmsnorm import rmsnorm_bwd_ref, rmsnorm_fwd_ref
-from .scan import scan_bwd_ref, scan_fwd_ref, scan_step_ref
+from .scan import (delta_softplus_ref, scan_bwd_fused_ref, scan_bwd_ref, scan_fwd_fused_ref, scan_fwd_ref,
+                   scan_step_ref)
 
 __all__ = [
-    "scan_fwd_ref", "scan_bwd_ref", "scan_step_ref", "conv1d_step_fwd_ref",
+    "scan_fwd_ref", "scan_bwd_ref", "scan_step_ref", "conv1d_step_fwd_ref", "delta_softplus_ref",
+    "scan_fwd_fused_ref", "scan_bwd_fused_ref",
     "conv1d_causal_fwd_ref", "conv1d_causal_silu_fwd_ref", "silu_ref", "dsilu_ref", "conv1d_causal_bwd_ref",
     "conv1d_causal_silu_bwd_ref", "conv1d_step_bwd_ref",
     "rmsnorm_fwd_ref", "rmsnorm_bwd_ref",

@@ -69,6 +69,39 @@ def scan_fwd_ref(x, delta, A, Bm, Cm, Dv, z, h0=None, chunk: int | None = None):
     return y, h, ckpt
 
 
+def delta_softplus_ref(delta_raw, dt_bias=None, softplus: bool = True):
+    """The discretisation step in front of the scan: delta = softplus(raw + dt_bias)
+    (softplus(v) = log(1 + e^v), evaluated as log(e^0 + e^v) by numpy.logaddexp),
+    or raw + dt_bias without the softplus.  dt_bias [D] or None (zero)."""
+    v = np.asarray(delta_raw, np.float64)
+    if dt_bias is not None:
+        v = v + np.asarray(dt_bias, np.float64)
+    return np.logaddexp(0.0, v) if softplus else v
+
+
+def scan_fwd_fused_ref(x, delta_raw, A, Bm, Cm, Dv, z, dt_bias=None, softplus: bool = True, h0=None,
+                       chunk: int | None = None):
+    """scan_fwd_ref on delta = delta_softplus_ref(delta_raw, dt_bias, softplus)."""
+    return scan_fwd_ref(x, delta_softplus_ref(delta_raw, dt_bias, softplus), A, Bm, Cm, Dv, z, h0=h0, chunk=chunk)
+
+
+def scan_bwd_fused_ref(x, delta_raw, A, Bm, Cm, Dv, z, dy, dt_bias=None, softplus: bool = True, h0=None,
+                       dh_last=None):
+    """Gradient through the fused discretisation: scan_bwd_ref on the transformed
+    delta, then the chain rule into the raw delta (softplus' = sigmoid) and the
+    bias (d dt_bias[d] = sum over b, t of that raw-delta gradient).  Returns the
+    scan_bwd_ref dict with 'ddelta' replaced and 'd_dt_bias' added."""
+    v = np.asarray(delta_raw, np.float64)
+    if dt_bias is not None:
+        v = v + np.asarray(dt_bias, np.float64)
+    delta = np.logaddexp(0.0, v) if softplus else v
+    g = dict(scan_bwd_ref(x, delta, A, Bm, Cm, Dv, z, dy, h0=h0, dh_last=dh_last))
+    if softplus:
+        g["ddelta"] = g["ddelta"] * _sigmoid(v)
+    g["d_dt_bias"] = np.sum(g["ddelta"], axis=(0, 1))
+    return g
+
+
 def scan_step_ref(h, x_t, delta_t, A, B_t, C_t, Dv, z_t):
     """One recurrent step for B sequences (the single-step updater of the
     rustytorch mamba_step_equivalence.rs test): h [B,D,N], x_t/delta_t/z_t [B,D],

@@ -57,7 +57,7 @@ def test_scan_fwd_validation(lib):
     p = [_fake(0x10000 + 256 * i) for i in range(11)]
 
     def call(ptrs=p, B=2, L=64, D=16, N=4, chunk=64, dtype=c.SS_F32):
-        return lib.ss_scan_fwd(*ptrs, B, L, D, N, chunk, dtype, None, 0, None)
+        return lib.ss_scan_fwd(*ptrs, B, L, D, N, chunk, dtype, None, 0, None, 0, None)
 
     q = list(p)
     q[0] = None
@@ -89,9 +89,10 @@ def test_scan_fwd_workspace(lib):
     assert lib.ss_scan_fwd_workspace_size(8, 2048, 4096, 16, 8, c.SS_BF16) == 0
     assert lib.ss_scan_fwd_workspace_size(2, 64, 16, 5, 64, c.SS_F32) == 0  # invalid N
     p = [_fake(0x10000 + 256 * i) for i in range(11)]
-    assert lib.ss_scan_fwd(*p, 2, 64, 16, 4, 64, c.SS_F32, None, 0, None) == c.SS_ERR_WORKSPACE
-    assert lib.ss_scan_fwd(*p, 2, 64, 16, 4, 64, c.SS_F32, _fake(0x90000), ws - 1, None) == c.SS_ERR_WORKSPACE
-    assert lib.ss_scan_fwd(*p, 2, 64, 16, 4, 64, c.SS_F32, _fake(0x90008), ws, None) == c.SS_ERR_ALIGN
+    f = lambda w, n: lib.ss_scan_fwd(*p, 2, 64, 16, 4, 64, c.SS_F32, None, 0, w, n, None)
+    assert f(None, 0) == c.SS_ERR_WORKSPACE
+    assert f(_fake(0x90000), ws - 1) == c.SS_ERR_WORKSPACE
+    assert f(_fake(0x90008), ws) == c.SS_ERR_ALIGN
 
 
 def test_scan_bwd_validation_and_workspace(lib):
@@ -105,7 +106,7 @@ def test_scan_bwd_validation_and_workspace(lib):
     p = [_fake(0x10000 + 256 * i) for i in range(18)]
 
     def call(ptrs=p, B=2, L=64, D=16, N=4, chunk=64, dtype=c.SS_F32, w=_fake(0x90000), wsz=ws):
-        return lib.ss_scan_bwd(*ptrs, B, L, D, N, chunk, dtype, w, wsz, None)
+        return lib.ss_scan_bwd(*ptrs, B, L, D, N, chunk, dtype, None, 0, None, w, wsz, None)
 
     q = list(p)
     q[8] = None  # dy

@@ -319,3 +319,46 @@ def test_scan_step_scalar_loop():
                 s += Ct[b, n] * hn
             yv = s * z[b, d] / (1 + math.exp(-z[b, d]))
             assert abs(yv - y[b, d]) <= 1e-12 * (1 + abs(yv))
+
+
+# ---------------------------------------------------------------- fused discretisation of delta
+
+
+def test_delta_softplus_definition_and_limits():
+    import math
+    from oracle import delta_softplus_ref
+    v = np.array([-30.0, -5.0, -1e-3, 0.0, 0.7, 5.0, 30.0, 80.0])
+    want = np.array([math.log1p(math.exp(t)) for t in v])
+    np.testing.assert_allclose(delta_softplus_ref(v), want, rtol=1e-15)
+    assert delta_softplus_ref(0.0) == math.log(2.0)
+    np.testing.assert_allclose(delta_softplus_ref(v, softplus=False), v, rtol=0)
+    np.testing.assert_allclose(delta_softplus_ref(np.zeros((1, 1, 2)), np.array([0.5, -0.5]), softplus=False)[0, 0],
+                               [0.5, -0.5])
+
+
+@pytest.mark.parametrize("softplus", [True, False])
+def test_fused_bwd_central_finite_differences(softplus):
+    """Central differences of the loss through delta = f(raw + dt_bias) in raw delta and dt_bias."""
+    from oracle import scan_bwd_fused_ref, scan_fwd_fused_ref
+    rng = np.random.default_rng(31 + softplus)
+    p = _rand_inputs(rng, B=2, L=5, D=3, N=2)
+    raw = rng.standard_normal((2, 5, 3)) * 0.5 - (2.0 if softplus else -0.3)
+    bias = rng.standard_normal(3) * 0.3
+    args = lambda: (p["x"], raw, p["A"], p["Bm"], p["Cm"], p["Dv"], p["z"])
+    g = scan_bwd_fused_ref(*args(), p["dy"], dt_bias=bias, softplus=softplus, h0=p["h0"])
+
+    def loss():
+        y, _, _ = scan_fwd_fused_ref(*args(), dt_bias=bias, softplus=softplus, h0=p["h0"])
+        return float(np.sum(y * p["dy"]))
+
+    for arr, gname in ((raw, "ddelta"), (bias, "d_dt_bias")):
+        fd = np.empty_like(arr)
+        for idx in np.ndindex(arr.shape):
+            v0 = arr[idx]
+            arr[idx] = v0 + 1e-6
+            lp = loss()
+            arr[idx] = v0 - 1e-6
+            lm = loss()
+            arr[idx] = v0
+            fd[idx] = (lp - lm) / 2e-6
+        assert max_rel_err(g[gname], fd) < 1e-7, gname

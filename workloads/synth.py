@@ -112,7 +112,9 @@ def make_scan_inputs(wl: Workload, seed: int = 0) -> dict:
 
     Returns float64 arrays (exactly representable in ``wl.dtype`` for the
     activations, in fp32 for A and Dv): ``x, delta, z, dy`` of shape [B,L,D],
-    ``Bm, Cm`` of shape [B,L,N], ``A`` [D,N], ``Dv`` [D], plus ``dt_bias`` [D].
+    ``Bm, Cm`` of shape [B,L,N], ``A`` [D,N], ``Dv`` [D], plus ``dt_bias`` [D] and
+    ``delta_raw`` [B,L,D] = 0.5*eps, the pre-bias, pre-softplus value whose
+    softplus(delta_raw + dt_bias) is ``delta`` before rounding.
     Draw order: dt_bias, eps, x, z, Bm, Cm, dy.
     """
     rng = _rng(seed, _STREAM_SCAN)
@@ -132,6 +134,7 @@ def make_scan_inputs(wl: Workload, seed: int = 0) -> dict:
     return {
         "x": r(x), "delta": r(delta), "z": r(z), "Bm": r(Bm), "Cm": r(Cm), "dy": r(dy),
         "A": round_to(A, "f32"), "Dv": round_to(Dv, "f32"), "dt_bias": round_to(dt_bias, "f32"),
+        "delta_raw": r(0.5 * eps),
     }
 
 
