@@ -10,6 +10,8 @@ namespace ssh {
 
 int read_clear_fwd_err(cudaStream_t s, unsigned* out);
 int read_clear_bwd_err(cudaStream_t s, unsigned* out);
+int read_clear_rms_err(cudaStream_t s, unsigned* out);
+int read_clear_rmsf_err(cudaStream_t s, unsigned* out);
 
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -61,8 +63,10 @@ extern "C" const char* ss_strerror(int code) {
 
 extern "C" int ss_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  unsigned a = 0, b = 0;
+  unsigned a = 0, b = 0, c = 0, d = 0;
   if (ssh::read_clear_fwd_err(s, &a) != SS_OK) return SS_ERR_CUDA;
   if (ssh::read_clear_bwd_err(s, &b) != SS_OK) return SS_ERR_CUDA;
-  return (a | b) ? SS_ERR_DEVICE : SS_OK;
+  if (ssh::read_clear_rms_err(s, &c) != SS_OK) return SS_ERR_CUDA;
+  if (ssh::read_clear_rmsf_err(s, &d) != SS_OK) return SS_ERR_CUDA;
+  return (a | b | c | d) ? SS_ERR_DEVICE : SS_OK;
 }

@@ -22,7 +22,7 @@ namespace {
 
 using namespace ssk;
 
-constexpr int kCTile = 64;     // time steps per tile
+constexpr int kCTile = 16;     // time steps per tile (short tiles: the (batch row, tile) items spread evenly over the CTAs)
 constexpr int kCThreads = 128;  // threads per CTA: 512 channels
 
 template <typename T>
@@ -171,7 +171,7 @@ inline ConvPlan conv_plan(int B, int L, int D, int K) {
   ConvPlan p;
   p.gx = (D / 4 + kCThreads - 1) / kCThreads;
   const long long pairs = (long long)B * ((L + kCTile - 1) / kCTile);
-  long long cap = 2048 / p.gx;
+  long long cap = 608 / p.gx;  // one wave: 4 resident CTAs on each of 152 SMs, each looping over its items
   if (cap < 1) cap = 1;
   p.gy = (int)(pairs < cap ? pairs : cap);
   p.bytes = (size_t)p.gy * D * (K + 1) * sizeof(float);

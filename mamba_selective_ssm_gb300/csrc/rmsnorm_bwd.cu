@@ -4,12 +4,15 @@
 //   dx[r,i] = inv (scale_i dy[r,i] - x[r,i] dot_r / dim);   dscale_i += sum_r dy x inv
 //
 // A CTA of T = ceil(dim / (8 VPT)) threads walks rows r = blockIdx.x, +gridDim.x, ...
-// Each thread owns VPT groups of 8 consecutive columns (16-byte bf16 or two
-// 16-byte fp32 loads), keeps scale and its dscale partial in registers, and
-// prefetches the next row while the current row's dot product is reduced
-// (warp shuffles, then one shared-memory exchange whose buffer alternates
-// with the row parity, so one barrier per row suffices).  Per-CTA dscale
-// partials are added in fixed order by colsum_kernel.
+// Each thread owns VPT groups of 8 consecutive columns, keeps scale and its
+// dscale partial in registers, and the row's dot product is reduced with warp
+// shuffles and one shared-memory exchange whose buffer alternates with the
+// row parity.  Rows reach the CTA through a ring of `nst` shared-memory stages
+// filled by untiled bulk copies (cp.async.bulk, one mbarrier per stage), so
+// up to nst rows of dy and x per CTA are in flight without holding registers
+// (rms_bwd_tma_kernel); the register-prefetch form (rms_bwd_kernel, one row
+// ahead) serves the fixed-grid no-alloc entry point and rows too wide for two
+// stages.  Per-CTA dscale partials are added in fixed order by colsum_kernel.
 #include <mutex>
 
 #include "common.cuh"
@@ -24,6 +27,8 @@ static __device__ __align__(256) float g_rms_noalloc_scratch[kNoAllocGrid * kNoA
 namespace {
 
 using namespace ssk;
+
+__device__ unsigned g_rms_err;
 
 constexpr int kRmsMaxThreads = 1024;
 constexpr int kRmsMaxDim = 32768;
@@ -109,6 +114,103 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_kernel(const T* __rest
   }
 }
 
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_tma_kernel(const T* __restrict__ dy, const T* __restrict__ x,
+                                                                     const float* __restrict__ scale,
+                                                                     const float* __restrict__ rms, float* __restrict__ dx,
+                                                                     float* __restrict__ ws, int rows, int dim, int nst) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  __shared__ float red[2][32];
+  const uint32_t row_bytes = (uint32_t)dim * sizeof(T);
+  T* buf = reinterpret_cast<T*>(sm);  // [nst][dy | x][dim]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)nst * 2 * row_bytes);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
+  const int nk = (rows - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // rows of this CTA
+  auto issue = [&](int k) {
+    const size_t r = (size_t)blockIdx.x + (size_t)k * gridDim.x;
+    const int st = k % nst;
+    mbar_arrive_expect_tx(&full[st], 2 * row_bytes);
+    bulk_load(buf + (size_t)(2 * st) * dim, dy + r * dim, row_bytes, &full[st]);
+    bulk_load(buf + (size_t)(2 * st + 1) * dim, x + r * dim, row_bytes, &full[st]);
+  };
+  if (tid == 0) {
+    for (int st = 0; st < nst; ++st) mbar_init(&full[st], 1);
+    fence_barrier_init();
+    for (int k = 0; k < nst && k < nk; ++k) issue(k);
+  }
+  float sc[VPT][8], acc[VPT][8];
+  bool col_ok[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = (v * blockDim.x + tid) * 8;
+    col_ok[v] = c < dim;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sc[v][e] = col_ok[v] ? scale[c + e] : 0.f;
+      acc[v][e] = 0.f;
+    }
+  }
+  __syncthreads();
+  const float inv_dim = 1.0f / (float)dim;
+  int parity = 0;
+  for (int k = 0; k < nk; ++k) {
+    const int r = (int)blockIdx.x + k * (int)gridDim.x;
+    const int st = k % nst;
+    bool ok = true;
+    if (tid == 0) ok = mbar_wait_bounded(&full[st], (k / nst) & 1, kWaitLimitNs);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicOr(&g_rms_err, kErrTmaTimeout);
+        for (int k2 = k; k2 < k + nst && k2 < nk; ++k2) mbar_wait_bounded(&full[k2 % nst], (k2 / nst) & 1, 100000000ull);
+      }
+      return;
+    }
+    float gy[VPT][8], xv[VPT][8];
+    float part = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = (v * blockDim.x + tid) * 8;
+      if (col_ok[v]) {
+        ActT<T>::ld8(buf + (size_t)(2 * st) * dim + c, gy[v]);
+        ActT<T>::ld8(buf + (size_t)(2 * st + 1) * dim + c, xv[v]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gy[v][e] = xv[v][e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) part = fmaf(gy[v][e] * sc[v][e], xv[v][e], part);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) red[parity][warp] = part;
+    __syncthreads();  // every thread has its row values: the stage can be refilled
+    if (tid == 0 && k + nst < nk) issue(k + nst);
+    float dot = 0.f;
+    for (int i = 0; i < nw; ++i) dot += red[parity][i];
+    parity ^= 1;
+    const float inv = 1.0f / rms[r];
+    const float kk = dot * inv * inv * inv_dim;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = (v * blockDim.x + tid) * 8;
+      if (col_ok[v]) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          o[e] = inv * (sc[v][e] * gy[v][e]) - inv * (xv[v][e] * kk);
+          acc[v][e] = fmaf(gy[v][e] * xv[v][e], inv, acc[v][e]);
+        }
+        ActT<float>::st8(dx + (size_t)r * dim + c, o);
+      }
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = (v * blockDim.x + tid) * 8;
+    if (col_ok[v]) ActT<float>::st8(ws + (size_t)blockIdx.x * dim + c, acc[v]);
+  }
+}
+
 struct AddTo {
   float* out;
   __device__ void put(long long i, float v) const { out[i] += v; }
@@ -135,6 +237,37 @@ int rms_validate(int rows, int dim, int dtype) {
   if (dim % 8 != 0) return SS_ERR_ALIGN;
   if (dim > kRmsMaxDim) return SS_ERR_DIM;
   return SS_OK;
+}
+
+// Shared-memory stages of the bulk-copy form (rows of at most 8192 columns, one
+// 8-column group per thread): ~100 KB per CTA (two CTAs per SM),
+// between 2 and 16 rows of dy and x; 0 when two stages do not fit.
+inline int rms_tma_stages(int dim, int esize) {
+  const size_t pair = (size_t)2 * dim * esize;
+  int nst = (int)((32u * 1024u) / pair);
+  if (nst > 16) nst = 16;
+  return nst >= 2 ? nst : 0;
+}
+
+template <typename T>
+int rms_tma_launch(const void* dy, const void* x, const float* scale, const float* rms, float* dx, float* dscale, int rows,
+                   int dim, float* ws, const RmsPlan& pl, int nst, cudaStream_t s) {
+  const size_t smem = (size_t)nst * 2 * dim * sizeof(T) + (size_t)nst * sizeof(uint64_t);
+  const T* g = static_cast<const T*>(dy);
+  const T* xx = static_cast<const T*>(x);
+  auto run = [&](auto kern) -> int {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, pl.threads, smem) != cudaSuccess || per_sm < 1)
+      return SS_ERR_CUDA;
+    int grid = per_sm * device_sm_count();
+    if (grid > pl.grid) grid = pl.grid;  // the workspace holds pl.grid partial rows
+    if (grid < 1) grid = 1;
+    kern<<<grid, pl.threads, smem, s>>>(g, xx, scale, rms, dx, ws, rows, dim, nst);
+    if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+    return colsum(ws, dim, grid, AddTo{dscale}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  };
+  return run(rms_bwd_tma_kernel<T, 1>);
 }
 
 template <typename T>
@@ -169,6 +302,11 @@ extern "C" int rmsnorm_bwd(const void* dy, const void* x, const float* scale, co
   if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* ws = static_cast<float*>(workspace);
+  const int nst = rms_tma_stages(dim, dtype == SS_F32 ? 4 : 2);
+  if (nst > 0 && pl.vpt == 1) {  // dim <= 8192 and two stages fit
+    if (dtype == SS_F32) return rms_tma_launch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, nst, s);
+    return rms_tma_launch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, nst, s);
+  }
   if (dtype == SS_F32) return rms_launch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
   return rms_launch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
 }
@@ -195,6 +333,15 @@ int noalloc_scratch(float** out) {
 }
 
 }  // namespace
+
+namespace ssh {
+int read_clear_rms_err(cudaStream_t s, unsigned* out) {
+  unsigned zero = 0;
+  if (cudaMemcpyFromSymbolAsync(out, g_rms_err, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SS_ERR_CUDA;
+  if (cudaMemcpyToSymbolAsync(g_rms_err, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, s) != cudaSuccess) return SS_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+}  // namespace ssh
 
 extern "C" int rmsnorm_bwd_noalloc(const void* dy, const void* x, const float* scale, const float* rms, float* dx,
                                    float* dscale, int rows, int dim, int dtype, void* stream) {

@@ -4,15 +4,19 @@
 //
 // Same row walk as the backward: a CTA of T = ceil(dim / (8 VPT)) threads
 // handles rows r = blockIdx.x, +gridDim.x, ...; each thread owns VPT groups of
-// 8 consecutive columns, prefetches the next row while the current row's sum
-// of squares is reduced (warp shuffles, then one shared-memory exchange whose
-// buffer alternates with the row parity), and writes y in the input dtype
-// (bf16 rounded to nearest even) and rms_r in fp32.
+// 8 consecutive columns; the row's sum of squares is reduced with warp
+// shuffles and one shared-memory exchange whose buffer alternates with the
+// row parity; y is written in the input dtype (bf16 rounded to nearest even)
+// and rms_r in fp32.  Rows of at most 8192 columns arrive through a ring of
+// shared-memory stages filled by untiled bulk copies (rms_fwd_tma_kernel);
+// wider rows use the register-prefetch form (one row ahead).
 #include "common.cuh"
 
 namespace {
 
 using namespace ssk;
+
+__device__ unsigned g_rmsf_err;
 
 constexpr int kRmsFMaxThreads = 1024;
 constexpr int kRmsFMaxDim = 32768;
@@ -85,6 +89,79 @@ __global__ void __launch_bounds__(kRmsFMaxThreads) rms_fwd_kernel(const T* __res
   }
 }
 
+template <typename T>
+__global__ void __launch_bounds__(kRmsFMaxThreads) rms_fwd_tma_kernel(const T* __restrict__ x,
+                                                                      const float* __restrict__ scale, float eps,
+                                                                      T* __restrict__ y, float* __restrict__ rms, int rows,
+                                                                      int dim, int nst) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  __shared__ float red[2][32];
+  const uint32_t row_bytes = (uint32_t)dim * sizeof(T);
+  T* buf = reinterpret_cast<T*>(sm);  // [nst][dim]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)nst * row_bytes);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
+  const int nk = (rows - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  auto issue = [&](int k) {
+    const size_t r = (size_t)blockIdx.x + (size_t)k * gridDim.x;
+    const int st = k % nst;
+    mbar_arrive_expect_tx(&full[st], row_bytes);
+    bulk_load(buf + (size_t)st * dim, x + r * dim, row_bytes, &full[st]);
+  };
+  if (tid == 0) {
+    for (int st = 0; st < nst; ++st) mbar_init(&full[st], 1);
+    fence_barrier_init();
+    for (int k = 0; k < nst && k < nk; ++k) issue(k);
+  }
+  const int c = tid * 8;
+  const bool col_ok = c < dim;
+  float sc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sc[e] = col_ok ? scale[c + e] : 0.f;
+  __syncthreads();
+  const float inv_dim = 1.0f / (float)dim;
+  int parity = 0;
+  for (int k = 0; k < nk; ++k) {
+    const int r = (int)blockIdx.x + k * (int)gridDim.x;
+    const int st = k % nst;
+    bool ok = true;
+    if (tid == 0) ok = mbar_wait_bounded(&full[st], (k / nst) & 1, kWaitLimitNs);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicOr(&g_rmsf_err, kErrTmaTimeout);
+        for (int k2 = k; k2 < k + nst && k2 < nk; ++k2) mbar_wait_bounded(&full[k2 % nst], (k2 / nst) & 1, 100000000ull);
+      }
+      return;
+    }
+    float xv[8];
+    if (col_ok) {
+      ActT<T>::ld8(buf + (size_t)st * dim + c, xv);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xv[e] = 0.f;
+    }
+    float part = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part = fmaf(xv[e], xv[e], part);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) red[parity][warp] = part;
+    __syncthreads();  // every thread has its row values: the stage can be refilled
+    if (tid == 0 && k + nst < nk) issue(k + nst);
+    float ss = 0.f;
+    for (int i = 0; i < nw; ++i) ss += red[parity][i];
+    parity ^= 1;
+    const float rr = sqrtf(fmaf(ss, inv_dim, eps));
+    const float inv = 1.0f / rr;
+    if (tid == 0 && rms != nullptr) rms[r] = rr;
+    if (col_ok) {
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = (xv[e] * sc[e]) * inv;
+      ActT<T>::st8(y + (size_t)r * dim + c, o);
+    }
+  }
+}
+
 int rms_fwd_validate(int rows, int dim, int dtype) {
   if (rows <= 0 || dim <= 0) return SS_ERR_DIM;
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
@@ -96,6 +173,22 @@ int rms_fwd_validate(int rows, int dim, int dtype) {
 template <typename T>
 int rms_fwd_launch(const void* x, const float* scale, float eps, void* y, float* rms, int rows, int dim, cudaStream_t s) {
   const int groups = dim / 8;
+  if (groups <= 1024) {  // one 8-column group per thread: the bulk-copy ring, up to 16 rows or ~100 KB per CTA
+    int nst = (int)((32u * 1024u) / ((size_t)dim * sizeof(T)));
+    if (nst > 16) nst = 16;
+    const int threads = (groups + 31) / 32 * 32;
+    const size_t smem = (size_t)nst * dim * sizeof(T) + (size_t)nst * sizeof(uint64_t);
+    auto kern = rms_fwd_tma_kernel<T>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+      return SS_ERR_CUDA;
+    int grid = per_sm * device_sm_count();
+    if (grid > rows) grid = rows;
+    if (grid < 1) grid = 1;
+    kern<<<grid, threads, smem, s>>>(static_cast<const T*>(x), scale, eps, static_cast<T*>(y), rms, rows, dim, nst);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  }
   const int vpt = groups <= 1024 ? 1 : groups <= 2048 ? 2 : 4;
   const int threads = ((groups + vpt - 1) / vpt + 31) / 32 * 32;
   const int grid = rows < 1216 ? rows : 1216;  // 8 CTAs per SM; each walks rows / 1216 rows
@@ -108,6 +201,17 @@ int rms_fwd_launch(const void* x, const float* scale, float eps, void* y, float*
 }
 
 }  // namespace
+
+namespace ssh {
+int read_clear_rmsf_err(cudaStream_t s, unsigned* out) {
+  unsigned zero = 0;
+  if (cudaMemcpyFromSymbolAsync(out, g_rmsf_err, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SS_ERR_CUDA;
+  if (cudaMemcpyToSymbolAsync(g_rmsf_err, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return SS_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+}  // namespace ssh
 
 extern "C" int rmsnorm_fwd(const void* x, const float* scale, float eps, void* y, float* rms, int rows, int dim, int dtype,
                            void* stream) {

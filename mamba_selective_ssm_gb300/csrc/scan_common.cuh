@@ -95,11 +95,4 @@ __device__ __forceinline__ void delta_transform4(float* dv, const float* bias_s,
   }
 }
 
-inline int device_sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 0;
-  return n;
-}
-
 }  // namespace ssk
