@@ -5,12 +5,13 @@
 //   dw[d,k] += sum_{b,t} dout[t,d] x[t-(K-1)+k, d],   db[d] += sum_{b,t} dout[t,d]
 //
 // A thread owns 4 adjacent channels (one 16-byte fp32 vector of dout per
-// step) over a 64-step tile of one batch row and slides two K-wide register
+// step) over a 16-step tile of one batch row and slides two K-wide register
 // windows along time: dout ahead of the output step (for dx) and x behind it
-// (for dw).  Each CTA loops over several (batch, tile) pairs, keeping dw / db
-// in registers, and writes one partial per CTA row; colsum_kernel adds
-// the partials in fixed order into dw / db.  HBM traffic is one read of dout
-// and x plus one write of dx (the K-1 halo steps per tile come from L2).
+// (for dw).  One wave of CTAs (four per SM, at most 128 registers a thread)
+// loops over the (batch, tile) items, keeping dw / db in registers, and writes
+// one partial per CTA row; colsum_kernel adds the partials in fixed order into
+// dw / db.  HBM traffic is one read of dout and x plus one write of dx (the
+// K-1 halo steps per tile come from L2).
 //
 // conv1d_causal_silu_bwd takes the gradient after a SiLU on the conv output
 // instead: the x window then reaches K-1 steps ahead as well, so that each
@@ -47,7 +48,7 @@ __device__ __forceinline__ float dsilu(float v) {
 }
 
 template <int K, typename T, bool SILU>
-__global__ void __launch_bounds__(kCThreads) conv_bwd_kernel(const float* __restrict__ dout, const T* __restrict__ x,
+__global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __restrict__ dout, const T* __restrict__ x,
                                                              const float* __restrict__ w, const float* __restrict__ bias,
                                                              float* __restrict__ dx, float* __restrict__ ws, int B, int L,
                                                              int D) {
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(kCThreads) conv_bwd_kernel(const float* __rest
         const int t = t0 + j;
         gw[j + 1] = t < L ? gact(*reinterpret_cast<const float4*>(g + (size_t)t * D), &xa[j + 1]) : f4z();
       }
-#pragma unroll 2
+#pragma unroll 8
       for (int s = t0; s < t1; ++s) {
 #pragma unroll
         for (int j = 0; j < 2 * K - 2; ++j) xa[j] = xa[j + 1];
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(kCThreads) conv_bwd_kernel(const float* __rest
         const int tx = t0 - (K - 1) + j;
         xw[j + 1] = tx >= 0 ? ld_x4(xb + (size_t)tx * D) : f4z();
       }
-#pragma unroll 4
+#pragma unroll 8
       for (int s = t0; s < t1; ++s) {
 #pragma unroll
         for (int j = 0; j < K - 1; ++j) {
