@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
       reinterpret_cast<float4*>(S.C_f)[gi] = make_float4(cv[0], cv[1], cv[2], cv[3]);
     }
     __syncthreads();
+    if (tid == 0 && k + NSTG < nitems) issue(k + NSTG);  // the slot is widened: refill it
 #pragma unroll
     for (int r = kTT - 1; r >= 0; --r) {
       const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[r * DT + dl]);
@@ -215,7 +216,6 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
       }
     }
     __syncthreads();
-    if (tid == 0 && k + NSTG < nitems) issue(k + NSTG);
   }
   if (dvalid) {
 #pragma unroll
@@ -821,6 +821,8 @@ template <typename T>
 struct Stages {
   static constexpr int value = 2;
 };
+// the summary kernel's tiles take a few hundred cycles each: six in flight
+constexpr int kSumStages = 6;
 
 template <int N, typename T, int NSTG, int DT, bool FUSE>
 int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, const void* dy,
@@ -880,8 +882,8 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
   int rows = pl.gy;
   if (p.P > 1) {
     rows = p.B * p.P;
-    const size_t smem_s = sizeof(BwdSumSmem<T, N, NSTG, DT>);
-    auto skern = scan_bwd_summary_kernel<N, T, NSTG, DT, FUSE>;
+    const size_t smem_s = sizeof(BwdSumSmem<T, N, kSumStages, DT>);
+    auto skern = scan_bwd_summary_kernel<N, T, kSumStages, DT, FUSE>;
     if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s) != cudaSuccess)
       return SS_ERR_CUDA;
     skern<<<dim3(pl.ndt, p.B * (p.P - 1)), Geo<N, DT>::NT, smem_s, stream>>>(p, tm[0], tm[2], tm[3], tm[5]);

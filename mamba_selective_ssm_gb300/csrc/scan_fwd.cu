@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_summary_kernel(
       reinterpret_cast<float4*>(S.B_f)[gi] = make_float4(bv[0], bv[1], bv[2], bv[3]);
     }
     __syncthreads();
+    if (tid == 0 && k + kNST < nitems) issue(k + kNST);  // the slot is widened: refill it
 #pragma unroll
     for (int r = 0; r < kTT; ++r) {
       const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
@@ -180,7 +181,6 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_summary_kernel(
       }
     }
     __syncthreads();
-    if (tid == 0 && k + kNST < nitems) issue(k + kNST);
   }
   if (dvalid) {
 #pragma unroll
