@@ -27,6 +27,31 @@ inline int device_sm_count() {
   return n;
 }
 
+// CTAs of `kern` that fit on one SM at `threads` threads and `smem` dynamic
+// shared-memory bytes, counted from the kernel's registers and shared memory
+// and the device's per-SM limits (registers allocated per warp in 256s, 1 KB of
+// shared memory reserved per CTA).  The runtime occupancy query returns 1 for
+// kernels that use tensor memory, which is not what the hardware schedules.
+template <typename K>
+inline int resident_ctas(K kern, int threads, size_t smem) {
+  cudaFuncAttributes fa;
+  int dev = 0, smem_sm = 0, regs_sm = 0, thr_sm = 0, blk_sm = 0;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess)
+    return 0;
+  const int warps = (threads + 31) / 32;
+  const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+  int n = blk_sm;
+  if (regs_warp > 0 && regs_sm / (regs_warp * warps) < n) n = regs_sm / (regs_warp * warps);
+  if (thr_sm / (warps * 32) < n) n = thr_sm / (warps * 32);
+  const size_t per_cta = smem + fa.sharedSizeBytes + 1024;
+  if ((int)((size_t)smem_sm / per_cta) < n) n = (int)((size_t)smem_sm / per_cta);
+  return n;
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

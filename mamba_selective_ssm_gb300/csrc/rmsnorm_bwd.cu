@@ -257,9 +257,12 @@ int rms_tma_launch(const void* dy, const void* x, const float* scale, const floa
   const T* xx = static_cast<const T*>(x);
   auto run = [&](auto kern) -> int {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
+  // prefer the largest shared-memory carveout, so that residency (and the occupancy
+  // query the segment and grid choices rely on) is limited by the CTAs' own needs
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, pl.threads, smem) != cudaSuccess || per_sm < 1)
-      return SS_ERR_CUDA;
+    per_sm = resident_ctas(kern, pl.threads, smem);
+    if (per_sm < 1) return SS_ERR_CUDA;
     int grid = per_sm * device_sm_count();
     if (grid > pl.grid) grid = pl.grid;  // the workspace holds pl.grid partial rows
     if (grid < 1) grid = 1;

@@ -180,9 +180,12 @@ int rms_fwd_launch(const void* x, const float* scale, float eps, void* y, float*
     const size_t smem = (size_t)nst * dim * sizeof(T) + (size_t)nst * sizeof(uint64_t);
     auto kern = rms_fwd_tma_kernel<T>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
+  // prefer the largest shared-memory carveout, so that residency (and the occupancy
+  // query the segment and grid choices rely on) is limited by the CTAs' own needs
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
-      return SS_ERR_CUDA;
+    per_sm = resident_ctas(kern, threads, smem);
+    if (per_sm < 1) return SS_ERR_CUDA;
     int grid = per_sm * device_sm_count();
     if (grid > rows) grid = rows;
     if (grid < 1) grid = 1;

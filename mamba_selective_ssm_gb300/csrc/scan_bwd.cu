@@ -855,8 +855,12 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
   // memory per CTA to keep the residency within that bound.
   size_t smem_launch = smem;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
+  // prefer the largest shared-memory carveout, so that residency (and the occupancy
+  // query the segment and grid choices rely on) is limited by the CTAs' own needs
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Geo<N, DT>::NT, smem) != cudaSuccess) return SS_ERR_CUDA;
+  per_sm = resident_ctas(kern, Geo<N, DT>::NT, smem);
+  if (per_sm < 1) return SS_ERR_CUDA;
   if (p.tcols != 0 && (uint32_t)per_sm * p.tcols > 512u) {
     const int max_ctas = 512 / (int)p.tcols;
     smem_launch = (size_t)(227 * 1024) / (size_t)(max_ctas + 1) + 1024;
@@ -864,8 +868,8 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
     if (smem_launch > 227 * 1024) smem_launch = 227 * 1024;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_launch) != cudaSuccess)
       return SS_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Geo<N, DT>::NT, smem_launch) != cudaSuccess)
-      return SS_ERR_CUDA;
+    per_sm = resident_ctas(kern, Geo<N, DT>::NT, smem_launch);
+    if (per_sm < 1) return SS_ERR_CUDA;
     if ((uint32_t)per_sm * p.tcols > 512u) return SS_ERR_UNSUPPORTED;
   }
   // segments: only when (batch row, channel tile) pairs leave resident CTA slots idle
@@ -886,6 +890,9 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
     auto skern = scan_bwd_summary_kernel<N, T, kSumStages, DT, FUSE>;
     if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s) != cudaSuccess)
       return SS_ERR_CUDA;
+  // prefer the largest shared-memory carveout, so that residency (and the occupancy
+  // query the segment and grid choices rely on) is limited by the CTAs' own needs
+  cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     skern<<<dim3(pl.ndt, p.B * (p.P - 1)), Geo<N, DT>::NT, smem_s, stream>>>(p, tm[0], tm[2], tm[3], tm[5]);
     if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
   }

@@ -461,14 +461,17 @@ int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, co
   const size_t smem = sizeof(FwdSmem<T, N, DT>);
   auto kern = scan_fwd_kernel<N, T, CPT, DT, FUSE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
+  // prefer the largest shared-memory carveout, so that residency (and the occupancy
+  // query the segment and grid choices rely on) is limited by the CTAs' own needs
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   // segments: only when (batch row, channel tile) pairs leave SMs idle
   p.P = 1;
   p.Ls = p.L;
   const int pmax = fwd_pmax<N>(p.B, p.L, p.D);
   if (pmax > 1) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, GeoF<N, CPT, DT>::NT, smem) != cudaSuccess)
-      return SS_ERR_CUDA;
+    per_sm = resident_ctas(kern, GeoF<N, CPT, DT>::NT, smem);
+    if (per_sm < 1) return SS_ERR_CUDA;
     const long long resident = (long long)per_sm * device_sm_count();
     int want = (int)(resident / ((long long)ndt * p.B));
     if (want > pmax) want = pmax;
@@ -483,6 +486,9 @@ int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, co
     auto skern = scan_fwd_summary_kernel<N, T, CPT, DT, FUSE>;
     if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s) != cudaSuccess)
       return SS_ERR_CUDA;
+  // prefer the largest shared-memory carveout, so that residency (and the occupancy
+  // query the segment and grid choices rely on) is limited by the CTAs' own needs
+  cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     skern<<<dim3(ndt, p.B * (p.P - 1)), GeoF<N, CPT, DT>::NT, smem_s, stream>>>(p, tm[0], tm[1], tm[3]);
     if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
     kern<<<dim3(ndt, p.B * p.P), GeoF<N, CPT, DT>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
