@@ -211,6 +211,66 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_tma_kernel(const T* __
   }
 }
 
+// Rows of at most 256 columns: G lanes per row (one 8-column group each), 32/G
+// rows per warp, the dot product reduced by shuffles inside each G-lane
+// segment, no block barrier per row.  The dscale partials of the CTA's
+// (warp, row slot) pairs are added in fixed order at the end.
+template <typename T, int G>
+__global__ void __launch_bounds__(256) rms_bwd_small_kernel(const T* __restrict__ dy, const T* __restrict__ x,
+                                                            const float* __restrict__ scale, const float* __restrict__ rms,
+                                                            float* __restrict__ dx, float* __restrict__ ws, int rows,
+                                                            int dim) {
+  constexpr int R = 32 / G;
+  __shared__ float red[8 * R][G * 8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int slot = lane / G, c = (lane % G) * 8;
+  const bool col_ok = c < dim;
+  float sc[8], acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sc[e] = col_ok ? scale[c + e] : 0.f;
+    acc[e] = 0.f;
+  }
+  const float inv_dim = 1.0f / (float)dim;
+  const long long step = (long long)gridDim.x * nw * R;
+  for (long long rb = ((long long)blockIdx.x * nw + warp) * R; rb < rows; rb += step) {
+    const long long r = rb + slot;
+    const bool row_ok = r < rows;
+    float gy[8], xv[8];
+    if (row_ok && col_ok) {
+      ActT<T>::ld8(dy + r * dim + c, gy);
+      ActT<T>::ld8(x + r * dim + c, xv);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) gy[e] = xv[e] = 0.f;
+    }
+    float part = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part = fmaf(gy[e] * sc[e], xv[e], part);
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (row_ok && col_ok) {
+      const float inv = 1.0f / rms[r];
+      const float kk = part * inv * inv * inv_dim;
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        o[e] = inv * (sc[e] * gy[e]) - inv * (xv[e] * kk);
+        acc[e] = fmaf(gy[e] * xv[e], inv, acc[e]);
+      }
+      ActT<float>::st8(dx + r * dim + c, o);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[warp * R + slot][(lane % G) * 8 + e] = acc[e];
+  __syncthreads();
+  for (int col = tid; col < dim; col += blockDim.x) {
+    float a = 0.f;
+    for (int i = 0; i < nw * R; ++i) a += red[i][col];
+    ws[(size_t)blockIdx.x * dim + col] = a;
+  }
+}
+
 struct AddTo {
   float* out;
   __device__ void put(long long i, float v) const { out[i] += v; }
@@ -237,6 +297,30 @@ int rms_validate(int rows, int dim, int dtype) {
   if (dim % 8 != 0) return SS_ERR_ALIGN;
   if (dim > kRmsMaxDim) return SS_ERR_DIM;
   return SS_OK;
+}
+
+template <typename T, int G>
+int rms_small_launch(const void* dy, const void* x, const float* scale, const float* rms, float* dx, float* dscale,
+                     int rows, int dim, float* ws, const RmsPlan& pl, cudaStream_t s) {
+  constexpr int R = 32 / G;
+  long long grid = ((long long)rows + 8 * R - 1) / (8 * R);
+  if (grid > pl.grid) grid = pl.grid;  // the workspace holds pl.grid partial rows
+  rms_bwd_small_kernel<T, G><<<(int)grid, 256, 0, s>>>(static_cast<const T*>(dy), static_cast<const T*>(x), scale, rms, dx,
+                                                       ws, rows, dim);
+  if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+  return colsum(ws, dim, (int)grid, AddTo{dscale}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+template <typename T>
+int rms_small_dispatch(const void* dy, const void* x, const float* scale, const float* rms, float* dx, float* dscale,
+                       int rows, int dim, float* ws, const RmsPlan& pl, cudaStream_t s) {
+  const int groups = dim / 8;
+  if (groups <= 1) return rms_small_launch<T, 1>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+  if (groups <= 2) return rms_small_launch<T, 2>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+  if (groups <= 4) return rms_small_launch<T, 4>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+  if (groups <= 8) return rms_small_launch<T, 8>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+  if (groups <= 16) return rms_small_launch<T, 16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+  return rms_small_launch<T, 32>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
 }
 
 // Shared-memory stages of the bulk-copy form (rows of at most 8192 columns, one
@@ -305,6 +389,10 @@ extern "C" int rmsnorm_bwd(const void* dy, const void* x, const float* scale, co
   if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* ws = static_cast<float*>(workspace);
+  if (dim <= 256) {  // short rows: several rows per warp
+    if (dtype == SS_F32) return rms_small_dispatch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+    return rms_small_dispatch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+  }
   const int nst = rms_tma_stages(dim, dtype == SS_F32 ? 4 : 2);
   if (nst > 0 && pl.vpt == 1) {  // dim <= 8192 and two stages fit
     if (dtype == SS_F32) return rms_tma_launch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, nst, s);

@@ -162,6 +162,63 @@ __global__ void __launch_bounds__(kRmsFMaxThreads) rms_fwd_tma_kernel(const T* _
   }
 }
 
+// Rows of at most 256 columns: G lanes per row (one 8-column group each), 32/G
+// rows per warp, the sum of squares reduced by shuffles inside each G-lane
+// segment, no block barrier per row.
+template <typename T, int G>
+__global__ void __launch_bounds__(256) rms_fwd_small_kernel(const T* __restrict__ x, const float* __restrict__ scale,
+                                                            float eps, T* __restrict__ y, float* __restrict__ rms, int rows,
+                                                            int dim) {
+  constexpr int R = 32 / G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int slot = lane / G, c = (lane % G) * 8;
+  const bool col_ok = c < dim;
+  float sc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sc[e] = col_ok ? scale[c + e] : 0.f;
+  const float inv_dim = 1.0f / (float)dim;
+  const long long step = (long long)gridDim.x * nw * R;
+  for (long long rb = ((long long)blockIdx.x * nw + warp) * R; rb < rows; rb += step) {
+    const long long r = rb + slot;
+    const bool row_ok = r < rows;
+    float xv[8];
+    if (row_ok && col_ok) {
+      ActT<T>::ld8(x + r * dim + c, xv);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xv[e] = 0.f;
+    }
+    float part = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part = fmaf(xv[e], xv[e], part);
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (row_ok) {
+      const float rr = sqrtf(fmaf(part, inv_dim, eps));
+      const float inv = 1.0f / rr;
+      if (c == 0 && rms != nullptr) rms[r] = rr;
+      if (col_ok) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = (xv[e] * sc[e]) * inv;
+        ActT<T>::st8(y + r * dim + c, o);
+      }
+    }
+  }
+}
+
+template <typename T, int G>
+int rms_fwd_small_launch(const void* x, const float* scale, float eps, void* y, float* rms, int rows, int dim,
+                         cudaStream_t s) {
+  constexpr int R = 32 / G;
+  long long grid = ((long long)rows + 8 * R - 1) / (8 * R);
+  const long long cap = 16ll * device_sm_count();
+  if (cap > 0 && grid > cap) grid = cap;
+  rms_fwd_small_kernel<T, G><<<(int)grid, 256, 0, s>>>(static_cast<const T*>(x), scale, eps, static_cast<T*>(y), rms, rows,
+                                                       dim);
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
 int rms_fwd_validate(int rows, int dim, int dtype) {
   if (rows <= 0 || dim <= 0) return SS_ERR_DIM;
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
@@ -173,6 +230,14 @@ int rms_fwd_validate(int rows, int dim, int dtype) {
 template <typename T>
 int rms_fwd_launch(const void* x, const float* scale, float eps, void* y, float* rms, int rows, int dim, cudaStream_t s) {
   const int groups = dim / 8;
+  if (groups <= 32) {  // short rows: several rows per warp
+    if (groups <= 1) return rms_fwd_small_launch<T, 1>(x, scale, eps, y, rms, rows, dim, s);
+    if (groups <= 2) return rms_fwd_small_launch<T, 2>(x, scale, eps, y, rms, rows, dim, s);
+    if (groups <= 4) return rms_fwd_small_launch<T, 4>(x, scale, eps, y, rms, rows, dim, s);
+    if (groups <= 8) return rms_fwd_small_launch<T, 8>(x, scale, eps, y, rms, rows, dim, s);
+    if (groups <= 16) return rms_fwd_small_launch<T, 16>(x, scale, eps, y, rms, rows, dim, s);
+    return rms_fwd_small_launch<T, 32>(x, scale, eps, y, rms, rows, dim, s);
+  }
   if (groups <= 1024) {  // one 8-column group per thread: the bulk-copy ring, up to 16 rows or ~100 KB per CTA
     int nst = (int)((32u * 1024u) / ((size_t)dim * sizeof(T)));
     if (nst > 16) nst = 16;
