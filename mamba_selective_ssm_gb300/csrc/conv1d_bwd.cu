@@ -52,8 +52,13 @@ __global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __r
                                                              const float* __restrict__ w, const float* __restrict__ bias,
                                                              float* __restrict__ dx, float* __restrict__ ws, int B, int L,
                                                              int D) {
-  const int d = (blockIdx.x * kCThreads + threadIdx.x) * 4;
-  const bool valid = d < D;  // D % 8 == 0, so all four channels are in range
+  // Rows narrower than a CTA (D/4 < kCThreads channel quads) pack ipc items per
+  // CTA step: thread slot `sub` takes every ipc-th item of its CTA row.
+  const int cpr = D / 4;
+  const int ipc = cpr >= kCThreads ? 1 : kCThreads / cpr;
+  const int sub = cpr >= kCThreads ? 0 : (int)threadIdx.x / cpr;
+  const int d = (cpr >= kCThreads ? (int)(blockIdx.x * kCThreads + threadIdx.x) : (int)threadIdx.x % cpr) * 4;
+  const bool valid = d < D && sub < ipc;  // D % 8 == 0, so all four channels are in range
   const int ntt = (L + kCTile - 1) / kCTile;
   float4 wk[K];  // wk[k] = w[d..d+3, k]
 #pragma unroll
@@ -74,7 +79,7 @@ __global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __r
   };
 
   if (valid && SILU) {
-    for (int bt = blockIdx.y; bt < B * ntt; bt += gridDim.y) {
+    for (int bt = blockIdx.y * ipc + sub; bt < B * ntt; bt += gridDim.y * ipc) {
       const int b = bt / ntt, t0 = (bt % ntt) * kCTile;
       const int t1 = min(L, t0 + kCTile);
       const float* g = dout + (size_t)b * L * D + d;
@@ -110,7 +115,7 @@ __global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __r
       }
     }
   } else if (valid) {
-    for (int bt = blockIdx.y; bt < B * ntt; bt += gridDim.y) {
+    for (int bt = blockIdx.y * ipc + sub; bt < B * ntt; bt += gridDim.y * ipc) {
       const int b = bt / ntt, t0 = (bt % ntt) * kCTile;
       const int t1 = min(L, t0 + kCTile);
       const float* g = dout + (size_t)b * L * D + d;
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __r
     }
   }
   if (valid) {
-    float* o = ws + (size_t)blockIdx.y * (K + 1) * D + d;  // partial row: [K+1][D]
+    float* o = ws + ((size_t)blockIdx.y * ipc + sub) * (K + 1) * D + d;  // partial row: [K+1][D]
 #pragma unroll
     for (int k = 0; k < K; ++k) *reinterpret_cast<float4*>(o + (size_t)k * D) = dw[k];
     *reinterpret_cast<float4*>(o + (size_t)K * D) = db;
@@ -164,7 +169,7 @@ struct ConvStore {
 };
 
 struct ConvPlan {
-  int gx, gy;
+  int gx, gy, rows;
   size_t bytes;
 };
 
@@ -174,8 +179,11 @@ inline ConvPlan conv_plan(int B, int L, int D, int K) {
   const long long pairs = (long long)B * ((L + kCTile - 1) / kCTile);
   long long cap = 608 / p.gx;  // one wave: 4 resident CTAs on each of 152 SMs, each looping over its items
   if (cap < 1) cap = 1;
-  p.gy = (int)(pairs < cap ? pairs : cap);
-  p.bytes = (size_t)p.gy * D * (K + 1) * sizeof(float);
+  const int ipc = D / 4 >= kCThreads ? 1 : kCThreads / (D / 4);  // items per CTA step (narrow rows)
+  const long long rows_needed = (pairs + ipc - 1) / ipc;
+  p.gy = (int)(rows_needed < cap ? rows_needed : cap);
+  p.rows = p.gy * ipc;  // partial rows: one per (CTA row, item slot)
+  p.bytes = (size_t)p.rows * D * (K + 1) * sizeof(float);
   return p;
 }
 
@@ -194,7 +202,7 @@ int conv_launch(const float* dout, const void* x, const float* w, const float* b
   conv_bwd_kernel<K, T, SILU>
       <<<dim3(pl.gx, pl.gy), kCThreads, 0, s>>>(dout, static_cast<const T*>(x), w, bias, dx, ws, B, L, D);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
-  return colsum(ws, (long long)D * (K + 1), pl.gy, ConvStore{dw, db, D, K}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  return colsum(ws, (long long)D * (K + 1), pl.rows, ConvStore{dw, db, D, K}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 }  // namespace

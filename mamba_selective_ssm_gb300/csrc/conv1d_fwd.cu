@@ -42,8 +42,12 @@ template <int K, typename T, bool SILU>
 __global__ void __launch_bounds__(kFThreads) conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w,
                                                              const float* __restrict__ bias, T* __restrict__ out, int B,
                                                              int L, int D) {
-  const int d = (blockIdx.x * kFThreads + threadIdx.x) * 4;
-  if (d >= D) return;  // D % 8 == 0: all four channels of a thread are in range
+  // rows narrower than a CTA pack ipc (batch row, tile) items per CTA step
+  const int cpr = D / 4;
+  const int ipc = cpr >= kFThreads ? 1 : kFThreads / cpr;
+  const int sub = cpr >= kFThreads ? 0 : (int)threadIdx.x / cpr;
+  const int d = (cpr >= kFThreads ? (int)(blockIdx.x * kFThreads + threadIdx.x) : (int)threadIdx.x % cpr) * 4;
+  if (d >= D || sub >= ipc) return;  // D % 8 == 0: all four channels of a thread are in range
   const int ntt = (L + kFTile - 1) / kFTile;
   float4 wk[K];
 #pragma unroll
@@ -51,7 +55,7 @@ __global__ void __launch_bounds__(kFThreads) conv_fwd_kernel(const T* __restrict
     wk[k] = make_float4(w[(size_t)d * K + k], w[(size_t)(d + 1) * K + k], w[(size_t)(d + 2) * K + k],
                         w[(size_t)(d + 3) * K + k]);
   const float4 b4 = bias != nullptr ? *reinterpret_cast<const float4*>(bias + d) : make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int bt = blockIdx.y; bt < B * ntt; bt += gridDim.y) {
+  for (int bt = blockIdx.y * ipc + sub; bt < B * ntt; bt += gridDim.y * ipc) {
     const int b = bt / ntt, t0 = (bt % ntt) * kFTile;
     const int t1 = min(L, t0 + kFTile);
     const T* xb = x + (size_t)b * L * D + d;
