@@ -151,3 +151,34 @@ def test_scan_rejects_misaligned_and_strided(ss):
     with pytest.raises(SSError) as e:
         ss.ss_scan_fwd(x_off, d["delta"], d["A"], d["Bm"], d["Cm"], d["Dv"], d["z"], chunk=64)
     assert e.value.code == -4
+
+
+@pytest.mark.parametrize("case", ["A_zero", "fast_decay", "saturated_gate", "zero_input"])
+def test_scan_degenerate_inputs(ss, case):
+    """Limits the recurrence meets in practice: no decay (a = 1: running sums), a strong decay (a down to
+    e^-100), a saturated gate (|z| large), and x = 0 (the state only decays).  The GPU path matches the oracle
+    and stays finite."""
+    wl = CONFIGS["tiny"].with_(B=2, L=150, D=40, N=16, dtype="f32", chunk=8)
+    inp = make_scan_inputs(wl, seed=13)
+    if case == "A_zero":
+        inp["A"] = np.zeros_like(inp["A"])
+    elif case == "fast_decay":
+        inp["A"] = inp["A"] * 20.0  # delta*A down to about -100 per step: the state forgets within a few steps
+    elif case == "saturated_gate":
+        inp["z"] = np.where(inp["z"] > 0, 60.0, -60.0)
+    else:
+        inp["x"] = np.zeros_like(inp["x"])
+    d = scan_inputs_on_device(inp, "f32")
+    res = run_gpu_scan(ss, d, 8)
+    _check_all(res, _oracle(inp, 8), TOL["f32"])
+    assert ss.device_status() == 0
+
+
+def test_scan_many_segments_long_row(ss):
+    """One batch row of 4096 steps over 32 channels: the sequence is cut into the maximum number of
+    segments (64), each composing its carry from all summaries before / after it."""
+    wl = CONFIGS["long"].with_(B=1, L=4096, D=32, N=16, dtype="bf16", chunk=8)
+    inp = make_scan_inputs(wl, seed=17)
+    d = scan_inputs_on_device(inp, "bf16")
+    res = run_gpu_scan(ss, d, 8)
+    _check_all(res, _oracle(inp, 8), TOL["bf16"])
