@@ -64,6 +64,27 @@ def algorithmic_bytes(wl, chunk):
     }
 
 
+# ex2.approx results per clock per SM: Blackwell Ultra doubled the special-function unit's exponential rate
+# to 32 (a chain of independent ex2.approx.ftz on GB300 delivers 31.4 per clock per SM at 2070 MHz)
+SFU_PER_CLK_PER_SM = 32
+
+
+def exp_co_bound(wl, ms, sms):
+    """The exponential pipe's bound beside the HBM roofline: the method takes one exp(delta*A) per (b, t, d, n)
+    in each direction (2*N per element), and the SFUs deliver SFU_PER_CLK_PER_SM results per clock per SM."""
+    mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    except Exception:
+        pass
+    exps = 2 * wl.B * wl.L * wl.D * wl.N
+    peak = SFU_PER_CLK_PER_SM * sms * mhz * 1e6
+    ach = exps / (ms * 1e-3)
+    return {"bound": "alu", "pipe": "MUFU ex2", "exps_per_step": exps, "achieved": ach, "peak": peak, "unit": "exp/s",
+            "frac": round(ach / peak, 4), "peak_from": f"{SFU_PER_CLK_PER_SM} per clock per SM x {sms} SMs x {mhz:.0f} MHz"}
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -376,6 +397,9 @@ def main():
                 "alg_bytes_per_launch": alg[dom]}
     scan_ms = per_call["scan_fwd"] + per_call["scan_bwd"]
     scan_bytes = alg["scan_fwd"] + alg["scan_bwd"]
+    # the same two calls with one checkpoint per 256 steps (fewer checkpoint bytes, same other traffic)
+    alg256 = algorithmic_bytes(wl, 256)
+    scan_bytes_256 = alg256["scan_fwd"] + alg256["scan_bwd"]
 
     # ---- the producers and fusions next to the hot path, each timed alone on the same tensors (L2 flushed)
     nxt = {}
@@ -517,7 +541,9 @@ def main():
             "roofline": roofline,
             "scan_fwd_bwd": {"ms": round(scan_ms, 5), "elems_per_s": elems / (scan_ms * 1e-3),
                              "alg_GB/s": round(scan_bytes / (scan_ms * 1e-3) / 1e9, 1),
-                             "frac": round(scan_bytes / (scan_ms * 1e-3) / 1e9 / peak, 4)},
+                             "frac": round(scan_bytes / (scan_ms * 1e-3) / 1e9 / peak, 4),
+                             "frac_at_chunk256_bytes": round(scan_bytes_256 / (scan_ms * 1e-3) / 1e9 / peak, 4),
+                             "exp_co_bound": exp_co_bound(wl, scan_ms, torch.cuda.get_device_properties(dev).multi_processor_count)},
             "kernels": kern, "next_kernels": nxt or None, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps,
         }), flush=True)

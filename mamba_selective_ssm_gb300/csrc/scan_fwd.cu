@@ -312,11 +312,15 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
         atomicOr(&g_fwd_err, kErrTmaTimeout);
-        for (int k2 = k; k2 < k + kNST && k2 < nitems; ++k2)
+        // copies in flight: items k .. k+kNST-1 before the first refill, k .. k+kNST-2 after it
+        const int kend = k + kNST - (k >= 1 ? 1 : 0);
+        for (int k2 = k; k2 < kend && k2 < nitems; ++k2)
           mbar_wait_bounded(&S.full[k2 % kNST], (k2 / kNST) & 1, 100000000ull);
       }
       return;
     }
+    // every thread is past the previous tile's epilogue: its staging slot can be refilled
+    if (tid == 0 && k >= 1 && k - 1 + kNST < nitems) issue(k - 1 + kNST);
 
     // widen the tile to fp32: delta, delta*x, B, C
     for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
@@ -414,8 +418,8 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
         }
       }
     }
-    __syncthreads();
-    if (tid == 0 && k + kNST < nitems) issue(k + kNST);
+    // no barrier here: the next tile's prologue writes only buffers this epilogue does not read,
+    // and its first barrier orders this epilogue before the next writes of yp and of the slot
     tck += kTT;
     if (tck >= p.chunk) tck -= p.chunk;
 
