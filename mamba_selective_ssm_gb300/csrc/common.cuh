@@ -145,6 +145,15 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Issued by the thread that is about to refill a shared-memory slot with an
+// async-proxy copy (TMA, bulk copy), after the barrier that follows the CTA's
+// last generic-proxy reads of that slot: it orders those reads before the
+// copy's writes.  Without it a refill can land while reads issued before the
+// barrier are still queued (seen as stale rows in a 4-slot TMA ring).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }

@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_tma_kernel(const T* __
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
   const int nk = (rows - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // rows of this CTA
   auto issue = [&](int k) {
+    fence_proxy_async_smem();  // the slot's earlier readers passed a barrier before this call
     const size_t r = (size_t)blockIdx.x + (size_t)k * gridDim.x;
     const int st = k % nst;
     mbar_arrive_expect_tx(&full[st], 2 * row_bytes);

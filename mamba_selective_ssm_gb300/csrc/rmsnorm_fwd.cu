@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kRmsFMaxThreads) rms_fwd_tma_kernel(const T* _
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
   const int nk = (rows - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   auto issue = [&](int k) {
+    fence_proxy_async_smem();  // the slot's earlier readers passed a barrier before this call
     const size_t r = (size_t)blockIdx.x + (size_t)k * gridDim.x;
     const int st = k % nst;
     mbar_arrive_expect_tx(&full[st], row_bytes);

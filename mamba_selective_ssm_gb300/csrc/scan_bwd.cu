@@ -68,7 +68,7 @@ struct BwdSmem {
 
 // Four 32-channel bf16 CTAs (N = 16, the register-limited residency) must also
 // fit the SM's 228 KB of shared memory, 1 KB of which each CTA reserves.
-static_assert(sizeof(BwdSmem<__nv_bfloat16, 16, 2, 32>) + 1024 <= 228 * 1024 / 4, "four backward CTAs per SM");
+static_assert(sizeof(BwdSmem<__nv_bfloat16, 16, 1, 32>) + 1024 <= 228 * 1024 / 4, "four backward CTAs per SM");
 
 // TMEM columns: 8 per window boundary of a chunk, rounded up to a power of two >= 32
 inline uint32_t tmem_cols(int chunk) {
@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
       Ap[j][q] = dvalid ? f2(a[0] * kLog2e, a[1] * kLog2e) : f2(0.f, 0.f);
     }
   auto issue = [&](int k) {
+    fence_proxy_async_smem();  // the slot's earlier readers passed a barrier before this call
     const int slot = k % NSTG, t0 = (gte - 1 - k) * kTT;
     mbar_arrive_expect_tx(&S.full[slot], kStageBytes);
     tma_load_3d(S.dlt[slot], &tm_dlt, &S.full[slot], d0, t0, b);
@@ -332,6 +333,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
   Cursor icur;
   start_row(icur, b_first);
   auto issue = [&](int k) {  // k: the item icur points at
+    fence_proxy_async_smem();  // the slot's earlier readers passed a barrier before this call
     const int b = icur.b, gt = tile_of(icur);
     const bool passB = icur.passB;
     advance(icur);
@@ -816,10 +818,11 @@ inline BwdPlan make_plan(int B, int L, int D, int N, int chunk) {
 }
 
 // pipeline depth: a staging slot is released right after the tile's widening
-// pass, so two slots keep one tile in flight during the tile's windows
+// pass and refilled with the next tile, which then lands during this tile's
+// windows: one slot suffices (two measured no faster, and cost 5 KB a CTA)
 template <typename T>
 struct Stages {
-  static constexpr int value = 2;
+  static constexpr int value = 1;
 };
 // the summary kernel's tiles take a few hundred cycles each: six in flight
 constexpr int kSumStages = 6;

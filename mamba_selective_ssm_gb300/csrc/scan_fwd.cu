@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_summary_kernel(
       Ap[j][q] = dvalid ? f2(a[0] * kLog2e, a[1] * kLog2e) : f2(0.f, 0.f);
     }
   auto issue = [&](int k) {
+    fence_proxy_async_smem();  // the slot's earlier readers passed a barrier before this call
     const int slot = k % kNST, t0 = tb + k * kTT;
     mbar_arrive_expect_tx(&S.full[slot], kStageBytes);
     tma_load_3d(S.dlt[slot], &tm_dlt, &S.full[slot], d0, t0, b);
@@ -256,6 +257,7 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
   }
 
   auto issue = [&](int k) {  // k: the item icur points at
+    fence_proxy_async_smem();  // the slot's earlier readers passed a barrier before this call
     const int slot = k % kNST;
     const int bb = icur.b;
     const int t0 = tb + icur.ti * kTT;

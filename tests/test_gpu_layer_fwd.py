@@ -26,7 +26,7 @@ def _bias(D, seed):
 @pytest.mark.parametrize("B,L,D,K,dtype,with_bias,silu", [
     (2, 64, 16, 4, "f32", True, False), (3, 130, 520, 4, "bf16", True, True), (2, 65, 24, 3, "f32", False, True),
     (1, 7, 8, 2, "bf16", True, True), (2, 33, 16, 1, "f32", True, False), (300, 40, 64, 4, "f32", False, True),
-    (1, 1, 8, 4, "f32", True, True),
+    (1, 1, 8, 4, "f32", True, True), (2, 97, 136, 3, "bf16", False, False), (1, 300, 8, 4, "bf16", True, True),
 ])
 def test_conv1d_fwd_parity(ss, B, L, D, K, dtype, with_bias, silu):
     wl = CONFIGS["tiny"].with_(B=B, L=L, D=D, d_conv=K, dtype=dtype)
