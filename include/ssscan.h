@@ -6,10 +6,9 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Every tensor argument is a caller-owned DEVICE pointer to a dense,
- *   row-major (C-contiguous) buffer; strided views are not accepted (a strided
- *   view silently read as contiguous is the bug the rustytorch backward_cuda
- *   commit message reports: "cuda_matmul reads raw GPU storage by shape.dims()
- *   ignoring strides/offset").  The library never allocates or frees memory
+ *   row-major (C-contiguous) buffer; strided views are not accepted (the
+ *   rustytorch backward_cuda commit message reports a GPU matmul that read a
+ *   strided view's storage as if it were dense).  The library never allocates or frees memory
  *   in these calls; scratch comes from the caller's `workspace`, sized by the
  *   matching *_workspace_size() query.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
@@ -69,8 +68,9 @@ size_t ss_scan_fwd_workspace_size(int B, int L, int D, int N, int chunk, int dty
  * ss_scan_fwd — selective-scan forward.
  *
  * The diagonal selective SSM trained by backpropagation through time in the
- * rustytorch MambaBlock ("the inherently sequential scan") and mamba-rs
- * ("BPTT through SSM state"); per batch b, channel d, state n, step t:
+ * rustytorch MambaBlock (whose scan runs step by step) and mamba-rs
+ * (backpropagation through time through the state); per batch b, channel d,
+ * state n, step t:
  *     a_t   = exp(delta_t[d] * A[d,n])
  *     h_t   = a_t * h_{t-1} + delta_t[d] * B_t[n] * x_t[d]        (h_{-1} = h0, or 0)
  *     y_t[d] = (sum_n C_t[n] * h_t[d,n] + D[d] * x_t[d]) * silu(z_t[d])

@@ -2,7 +2,7 @@
 
 Definition (the diagonal selective SSM the pages train by backpropagation
 through time; rustytorch ``backward_cuda`` commit message, mamba-rs crate
-description "BPTT through SSM state"):
+description):
 
     a_t[d,n] = exp(delta_t[d] * A[d,n])
     h_t[d,n] = a_t[d,n] * h_{t-1}[d,n] + delta_t[d] * B_t[n] * x_t[d]     (h_{-1} = h0, else 0)

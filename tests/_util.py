@@ -3,9 +3,9 @@
 import numpy as np
 
 # Per-tensor infinity-norm relative error, max_i |g_i - r_i| / max_i |r_i|.  The
-# rustytorch backward_cuda commit quotes a "max relative error" tolerance of
-# 1e-4 between GPU and CPU gradients without defining it; this is the reading
-# taken.  bf16 activations (with fp32 state and grads) get 2e-2.
+# rustytorch backward_cuda commit gives a 1e-4 bound on the relative error
+# between GPU and CPU gradients without defining the metric; this is the
+# reading taken.  bf16 activations (with fp32 state and grads) get 2e-2.
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 
 
