@@ -336,7 +336,7 @@ def main():
         "rmsnorm_bwd": lambda: lib.rmsnorm_bwd(p(X["r_dy"]), p(X["r_x"]), p(X["r_scale"]), p(X["r_rms"]),
                                                p(O["r_dx"]), p(O["r_dscale"]), B * L, H, sdt, p(W), wsz, sp),
     }
-    launches_per_step = 1 + 3 + 2 + 2  # fwd; bwd + dB/dC sum + dA/dD sum; conv + sum; rms + sum
+    launches_per_step = 1 + 2 + 2 + 2  # fwd; bwd + its reductions (dB/dC and dA/dD in one launch); conv + sum; rms + sum
     names = list(calls)
 
     def step(ev=None):

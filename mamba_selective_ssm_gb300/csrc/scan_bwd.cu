@@ -18,7 +18,7 @@
 // shares to shared memory; the window epilogue adds the shares in a fixed
 // order (over the 4-state lane groups for the per-(t,d) sums, over lanes and
 // warps for dB_t, dC_t) and writes dx, ddelta, dz and one dB/dC partial per
-// channel tile.  ss_bwd_dbc_kernel and colsum_kernel add the partials of
+// channel tile.  ss_bwd_reduce_kernel adds the partials of
 // dB/dC and of dA/dD in fixed order.  No atomics: results are bitwise
 // reproducible.
 #include "scan_common.cuh"
@@ -759,19 +759,6 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
   }
 }
 
-// dB, dC = sum over the 64-channel tiles in tile order (overwrite).
-template <int N>
-__global__ void ss_bwd_dbc_kernel(const float* __restrict__ ws_dBC, float* dB, float* dC, long long nBC, int ndt) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nBC; i += (long long)gridDim.x * blockDim.x) {
-    float acc = 0.f;
-    for (int t = 0; t < ndt; ++t) acc += ws_dBC[(size_t)t * nBC + i];
-    const long long row = i / (2 * N);
-    const int c = (int)(i % (2 * N));
-    if (c < N) dB[row * N + c] = acc;
-    else dC[row * N + (c - N)] = acc;
-  }
-}
-
 // dA (first D*N columns of a partial row), dD (next D) and d dt_bias (last D,
 // when asked for) accumulate.
 struct DADStore {
@@ -785,6 +772,43 @@ struct DADStore {
     else if (dT != nullptr) dT[i - nA - D] += v;
   }
 };
+
+// The backward's fixed-order reductions in one launch.  Blocks [0, nblk_bc):
+// dB, dC = sum over the channel tiles' partials in tile order (overwrite).
+// The other blocks: 32 columns of the dA / dD / d dt_bias partial rows each;
+// thread (x, y) adds rows y, y+8, ... in ascending order, then the eight sums
+// are added y = 0..7 (the order colsum_kernel uses).
+template <int N>
+__global__ void __launch_bounds__(256) ss_bwd_reduce_kernel(const float* __restrict__ ws_dBC, float* dB, float* dC,
+                                                            long long nBC, int ndt, int nblk_bc,
+                                                            const float* __restrict__ ws_dAD, long long nAD, int rows,
+                                                            DADStore st) {
+  if ((int)blockIdx.x < nblk_bc) {
+    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < nBC; i += (long long)nblk_bc * 256) {
+      float acc = 0.f;
+      for (int t = 0; t < ndt; ++t) acc += ws_dBC[(size_t)t * nBC + i];
+      const long long row = i / (2 * N);
+      const int c = (int)(i % (2 * N));
+      if (c < N) dB[row * N + c] = acc;
+      else dC[row * N + (c - N)] = acc;
+    }
+    return;
+  }
+  __shared__ float red[8][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const long long i = (long long)(blockIdx.x - nblk_bc) * 32 + tx;
+  float acc = 0.f;
+  if (i < nAD)
+    for (int g = ty; g < rows; g += 8) acc += ws_dAD[(size_t)g * nAD + i];
+  red[ty][tx] = acc;
+  __syncthreads();
+  if (ty == 0 && i < nAD) {
+    float v = red[0][tx];
+#pragma unroll
+    for (int y = 1; y < 8; ++y) v += red[y][tx];
+    st.put(i, v);
+  }
+}
 
 // Channels per CTA of a launch: with a recompute pass (chunk > 8) the TMEM
 // columns a CTA holds grow with the chunk; from 128 columns (at most four CTAs
@@ -902,13 +926,13 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
   kern<<<dim3(pl.ndt, rows), Geo<N, DT>::NT, smem_launch, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4], tm[5]);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
   const long long nBC = (long long)p.B * p.L * 2 * N;
-  long long blocks = (nBC + 255) / 256;
-  if (blocks > 8192) blocks = 8192;
-  ss_bwd_dbc_kernel<N><<<(int)blocks, 256, 0, stream>>>(p.ws_dBC, dB, dC, nBC, pl.ndt);
-  if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
-  const long long nA = (long long)p.D * N;
-  return colsum(p.ws_dAD, nA + 2ll * p.D, rows, DADStore{dA, dD, p.d_dt_bias, nA, p.D}, stream) == cudaSuccess ? SS_OK
-                                                                                                      : SS_ERR_CUDA;
+  long long blk_bc = (nBC + 255) / 256;
+  if (blk_bc > 8192) blk_bc = 8192;
+  const long long nA = (long long)p.D * N, nAD = nA + 2ll * p.D;
+  const long long blk_ad = (nAD + 31) / 32;
+  ss_bwd_reduce_kernel<N><<<(unsigned)(blk_bc + blk_ad), 256, 0, stream>>>(
+      p.ws_dBC, dB, dC, nBC, pl.ndt, (int)blk_bc, p.ws_dAD, nAD, rows, DADStore{dA, dD, p.d_dt_bias, nA, p.D});
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 // the discretisation of delta is a template switch, so the plain scan carries none of it
