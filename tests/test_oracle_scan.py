@@ -362,3 +362,45 @@ def test_fused_bwd_central_finite_differences(softplus):
             arr[idx] = v0
             fd[idx] = (lp - lm) / 2e-6
         assert max_rel_err(g[gname], fd) < 1e-7, gname
+
+
+def test_two_step_example_worked_by_hand():
+    """B = 1, D = 1, N = 2, L = 2, worked from the recurrence by hand.
+
+    delta = 1 and A = (-ln 2, -2 ln 2) give a_t = (1/2, 1/4); x = (1, 2),
+    B_0 = (1, 2), B_1 = (3, -1), C_0 = (1, 1), C_1 = (2, 1), D = 1/2,
+    z = ln 3 (sigmoid 3/4, silu = (3/4) ln 3), dy = 1, h starts at 0:
+      h_0 = (1, 2),  h_1 = (1/2, 1/2) + 2 (3, -1) = (6.5, -1.5)
+      s_0 = 3 + 1/2 = 3.5,  s_1 = 13 - 1.5 + 1 = 12.5,  y_t = s_t (3/4) ln 3
+    Backward with g = ds_t = (3/4) ln 3:
+      G_1 = g (2, 1),  G_0 = g (1, 1) + a_1 G_1 = g (2, 1.25)
+      q_1 = a_1 G_1 h_0 = g (1, 0.5),  q_0 = 0 (h before step 0 is 0)
+      dx_t = g D + sum_n G_t B_t           -> g (5, 5.5)
+      ddelta_t = sum_n (q_t A + G_t B_t x_t) -> g (4.5, 10 - 2 ln 2)
+      dA = sum_t q_t delta_t = g (1, 0.5);  dB_t = G_t x_t;  dC_t = g h_t;  dD = g (1 + 2)
+      dz_t = s_t sigmoid(z) (1 + z (1 - sigmoid(z))) = s_t (3/4) (1 + ln 3 / 4)
+      dh0 = a_0 G_0 = g (1, 0.3125)
+    """
+    ln2, ln3 = np.log(2.0), np.log(3.0)
+    x = np.array([[[1.0], [2.0]]])
+    delta = np.ones((1, 2, 1))
+    A = np.array([[-ln2, -2 * ln2]])
+    Bm = np.array([[[1.0, 2.0], [3.0, -1.0]]])
+    Cm = np.array([[[1.0, 1.0], [2.0, 1.0]]])
+    Dv = np.array([0.5])
+    z = np.full((1, 2, 1), ln3)
+    dy = np.ones((1, 2, 1))
+    y, h_last, _ = scan_fwd_ref(x, delta, A, Bm, Cm, Dv, z)
+    g = 0.75 * ln3
+    tol = 1e-12
+    assert max_rel_err(y[0, :, 0], [3.5 * g, 12.5 * g]) < tol
+    assert max_rel_err(h_last[0, 0], [6.5, -1.5]) < tol
+    r = scan_bwd_ref(x, delta, A, Bm, Cm, Dv, z, dy)
+    assert max_rel_err(r["dx"][0, :, 0], [5 * g, 5.5 * g]) < tol
+    assert max_rel_err(r["ddelta"][0, :, 0], [4.5 * g, (10 - 2 * ln2) * g]) < tol
+    assert max_rel_err(r["dz"][0, :, 0], [3.5 * 0.75 * (1 + ln3 / 4), 12.5 * 0.75 * (1 + ln3 / 4)]) < tol
+    assert max_rel_err(r["dA"][0], [g, 0.5 * g]) < tol
+    assert max_rel_err(r["dB"][0], [[2 * g, 1.25 * g], [4 * g, 2 * g]]) < tol
+    assert max_rel_err(r["dC"][0], [[g, 2 * g], [6.5 * g, -1.5 * g]]) < tol
+    assert max_rel_err(r["dD"], [3 * g]) < tol
+    assert max_rel_err(r["dh0"][0, 0], [g, 0.3125 * g]) < tol
