@@ -107,3 +107,35 @@ def test_conv_rms_repeat_bitwise(ss):
     torch.cuda.synchronize()
     assert ss.device_status() == 0
     _same(torch, runs, "conv/rmsnorm")
+
+
+def test_scan_fullsize_halves_chain_to_the_whole(ss):
+    """Every element at full size: the 1.4B layer's scan over L = 2048 equals its two halves chained through
+    h_last -> h0 (forward) and dh0 -> dh_last (backward).  Both ways run the same per-thread recurrence, so the
+    per-step outputs agree to rounding (1e-5 here); dA and dD are sums over both halves in another order."""
+    import torch
+    B, L, D, N, chunk = 4, 2048, 4096, 16, 8
+    t = _layer(torch, B, L, D, N, torch.bfloat16, seed=24)
+    args = lambda sl: [t[k][:, sl].contiguous() if k in ("x", "delta", "z", "Bm", "Cm") else t[k] for k in ("x", "delta", "A", "Bm", "Cm", "Dv", "z")]
+    full, first, second = slice(0, L), slice(0, L // 2), slice(L // 2, L)
+    y, ck, hl = ss.ss_scan_fwd(*args(full), chunk=chunk)
+    g = ss.ss_scan_bwd(*args(full), ck, t["dy"], chunk=chunk)
+    ya, cka, ha = ss.ss_scan_fwd(*args(first), chunk=chunk)
+    yb, ckb, hb = ss.ss_scan_fwd(*args(second), h0=ha, chunk=chunk)
+    gb = ss.ss_scan_bwd(*args(second), ckb, t["dy"][:, second].contiguous(), chunk=chunk)
+    ga = ss.ss_scan_bwd(*args(first), cka, t["dy"][:, first].contiguous(), dh_last=gb["dh0"], chunk=chunk)
+    torch.cuda.synchronize()
+    assert ss.device_status() == 0
+
+    def rel(a, b):
+        a, b = a.float(), b.float()
+        return float((a - b).abs().max() / b.abs().max().clamp_min(1e-30))
+
+    tol = 1e-5
+    assert rel(torch.cat([ya, yb], 1), y) <= 2e-2  # bf16 outputs: at most one rounding step apart
+    assert rel(hb, hl) <= tol
+    for k in ("dx", "ddelta", "dz", "dB", "dC"):
+        assert rel(torch.cat([ga[k], gb[k]], 1), g[k]) <= tol, k
+    assert rel(ga["dh0"], g["dh0"]) <= tol
+    assert rel(ga["dA"] + gb["dA"], g["dA"]) <= 1e-4
+    assert rel(ga["dD"] + gb["dD"], g["dD"]) <= 1e-4
