@@ -325,8 +325,8 @@ int rms_small_dispatch(const void* dy, const void* x, const float* scale, const 
 }
 
 // Shared-memory stages of the bulk-copy form (rows of at most 8192 columns, one
-// 8-column group per thread): ~100 KB per CTA (two CTAs per SM),
-// between 2 and 16 rows of dy and x; 0 when two stages do not fit.
+// 8-column group per thread): ~32 KB per CTA, between 2 and 16 rows of dy and
+// x; 0 when two stages do not fit.
 inline int rms_tma_stages(int dim, int esize) {
   const size_t pair = (size_t)2 * dim * esize;
   int nst = (int)((32u * 1024u) / pair);
