@@ -298,6 +298,21 @@ int conv1d_causal_step(const void* x, float* conv_state, const float* w, const f
                        int B, int D, int d_conv, int silu, int dtype, void* stream);
 
 /*
+ * ss_count_nonfinite — failure detection: writes to `count` (a device
+ * uint64) the number of NaN and +-Inf values among the n elements of `p`
+ * (dtype SS_F32 or SS_BF16; a value counts when its exponent field is all
+ * ones).  A caller checks a step's gradients with it and drops the step when
+ * the count is nonzero.  The count is exact and independent of the launch
+ * (two fixed-order integer passes, no atomics).
+ *   p         : device buffer, 16-byte aligned (NULL allowed when n == 0)
+ *   count     : device, 8-byte aligned, overwritten
+ *   workspace : ss_count_nonfinite_workspace_size() bytes, 16-byte aligned
+ */
+size_t ss_count_nonfinite_workspace_size(void);
+int ss_count_nonfinite(const void* p, size_t n, int dtype, unsigned long long* count, void* workspace,
+                       size_t ws_bytes, void* stream);
+
+/*
  * ss_device_status — synchronises `stream`, then reads and clears the
  * library's device-side error word.  Returns SS_OK, or SS_ERR_DEVICE when a
  * kernel gave up on a bounded wait for its own asynchronous copies since the

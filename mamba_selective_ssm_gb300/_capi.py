@@ -44,6 +44,8 @@ SIGNATURES = {
     "rmsnorm_fwd": (_i, [_vp, _vp, ctypes.c_float, _vp, _vp, _i, _i, _i, _vp]),
     "ss_scan_step": (_i, [_vp] * 9 + [_i] * 4 + [_vp]),
     "conv1d_causal_step": (_i, [_vp] * 5 + [_i] * 5 + [_vp]),
+    "ss_count_nonfinite_workspace_size": (_sz, []),
+    "ss_count_nonfinite": (_i, [_vp, _sz, _i, _vp, _vp, _sz, _vp]),
     "ss_device_status": (_i, [_vp]),
 }
 

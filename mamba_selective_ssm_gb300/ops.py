@@ -293,6 +293,20 @@ def conv1d_causal_step(x, conv_state, w, bias=None, silu: bool = False):
     return out
 
 
+def count_nonfinite(t, workspace=None) -> int:
+    """Number of NaN / +-Inf values in a dense fp32 or bf16 CUDA tensor (synchronises the current stream)."""
+    lib = load()
+    dt = _act_dtype(t)
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("count_nonfinite: t must be a contiguous CUDA tensor")
+    wsz = lib.ss_count_nonfinite_workspace_size()
+    ws = workspace if workspace is not None else torch.empty((wsz,), device=t.device, dtype=torch.uint8)
+    out = torch.empty((1,), device=t.device, dtype=torch.int64)
+    rc = lib.ss_count_nonfinite(_p(t), t.numel(), dt, _p(out), _p(ws), ws.numel() * ws.element_size(), _stream())
+    check(rc, "ss_count_nonfinite")
+    return int(out.item())
+
+
 def device_status() -> int:
     """Reads and clears the library's device error word (synchronises the current stream)."""
     return load().ss_device_status(_stream())

@@ -197,3 +197,18 @@ def test_wrapper_rejects_strided_and_cpu_tensors():
     t = torch.zeros(4, 4)
     with pytest.raises(ValueError, match="CUDA"):
         ops._req(t, "x")
+
+
+def test_count_nonfinite_validation(lib):
+    from mamba_selective_ssm_gb300 import _capi as c
+    wsz = lib.ss_count_nonfinite_workspace_size()
+    assert wsz >= 4096
+    f = lambda p=_fake(0x50000), n=100, dt=c.SS_F32, cnt=_fake(0x60000), w=_fake(0x70000), ws=wsz: \
+        lib.ss_count_nonfinite(p, n, dt, cnt, w, ws, None)
+    assert f(cnt=None) == c.SS_ERR_NULL
+    assert f(p=None) == c.SS_ERR_NULL
+    assert f(dt=7) == c.SS_ERR_UNSUPPORTED
+    assert f(w=None) == c.SS_ERR_WORKSPACE
+    assert f(ws=wsz - 4) == c.SS_ERR_WORKSPACE
+    assert f(p=_fake(0x50004)) == c.SS_ERR_ALIGN
+    assert f(cnt=_fake(0x60004)) == c.SS_ERR_ALIGN
