@@ -212,3 +212,21 @@ def test_count_nonfinite_validation(lib):
     assert f(ws=wsz - 4) == c.SS_ERR_WORKSPACE
     assert f(p=_fake(0x50004)) == c.SS_ERR_ALIGN
     assert f(cnt=_fake(0x60004)) == c.SS_ERR_ALIGN
+
+
+def test_abi_is_usable_from_plain_c(lib, tmp_path):
+    """tests/abi_from_c.c includes include/ssscan.h and links libssscan.so with gcc: no Python or torch types
+    cross the boundary."""
+    import subprocess
+    from mamba_selective_ssm_gb300 import _build
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(_build.LIB_PATH)
+    exe = tmp_path / "abi_from_c"
+    src = os.path.join(ROOT, "tests", "abi_from_c.c")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src, "-o", str(exe),
+                        "-L", libdir, "-lssscan", f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
