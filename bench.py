@@ -54,7 +54,7 @@ def algorithmic_bytes(wl, chunk):
     B, L, D, N, K, H = wl.B, wl.L, wl.D, wl.N, wl.d_conv, wl.d_model
     E = B * L * D
     nck = -(-L // chunk)
-    ck = B * D * nck * N * 4
+    ck = B * D * (nck - 1) * N * 4  # checkpoints after the first (the first is the initial state)
     small = (D * N + D) * 4
     return {
         "scan_fwd": E * 4 * e + B * L * N * 2 * e + ck + small,
