@@ -43,18 +43,26 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip timing the kernels next to the hot path")
+    ap.add_argument("--no-others", action="store_true", help="skip timing the scan on the other workloads")
     return ap.parse_args()
 
 
 # ---------------------------------------------------------------- accounting
 
-def algorithmic_bytes(wl, chunk):
-    """Bytes each call must move (scratch excluded): reads of its inputs, writes of its outputs."""
+# The method's own checkpoint interval for the byte count: one checkpoint per 256 steps (the long-context
+# workload's interval).  A kernel run at a shorter interval moves more checkpoint bytes; those are reported as
+# overhead, not as algorithmic work.
+ALG_CHUNK = 256
+
+
+def algorithmic_bytes(wl, chunk=ALG_CHUNK):
+    """Bytes each call must move (scratch excluded): reads of its inputs, writes of its outputs; the scan's
+    checkpoints are counted after the first (the first is the initial state) at one per `chunk` steps."""
     e = 2 if wl.dtype == "bf16" else 4
     B, L, D, N, K, H = wl.B, wl.L, wl.D, wl.N, wl.d_conv, wl.d_model
     E = B * L * D
     nck = -(-L // chunk)
-    ck = B * D * (nck - 1) * N * 4  # checkpoints after the first (the first is the initial state)
+    ck = B * D * (nck - 1) * N * 4
     small = (D * N + D) * 4
     return {
         "scan_fwd": E * 4 * e + B * L * N * 2 * e + ck + small,
@@ -64,25 +72,49 @@ def algorithmic_bytes(wl, chunk):
     }
 
 
-# ex2.approx results per clock per SM: Blackwell Ultra doubled the special-function unit's exponential rate
-# to 32 (a chain of independent ex2.approx.ftz on GB300 delivers 31.4 per clock per SM at 2070 MHz)
+def checkpoint_overhead_bytes(wl, chunk):
+    """Checkpoint bytes one scan call moves beyond the algorithmic count: the forward writes, and the backward
+    reads, all ceil(L/chunk) checkpoints (the first included), where the count allows ceil(L/256) - 1."""
+    moved = wl.B * wl.D * (-(-wl.L // chunk)) * wl.N * 4
+    counted = wl.B * wl.D * (-(-wl.L // ALG_CHUNK) - 1) * wl.N * 4
+    return moved - counted
+
+
+# FP32 operations per (b, t, d, n) cell on the recurrence (fused multiply-adds and multiplies, one each):
+# forward  delta*A, delta*x*B, the state update, the C.h sum                                   -> 4
+# backward the rebuild (delta*A, delta*x*B, update), G, a*G, q = aG*h, q*A, G*B, C*h, dA, dB, dC -> 12
+FP32_OPS_PER_CELL = {"scan_fwd": 4, "scan_bwd": 12}
+
+
+# Unit rates per SM per clock on GB300, measured on this pool by throughput probes (independent chains, one CTA
+# per SM): ex2.approx.ftz 32 results (1.0 warp instruction), FP32 fused multiply-add 123 lanes (packed f32x2
+# issues at 1.93 warp instructions per clock, each two lanes' work).
 SFU_PER_CLK_PER_SM = 32
+FMA_PER_CLK_PER_SM = 123
 
 
-def exp_co_bound(wl, ms, sms):
-    """The exponential pipe's bound beside the HBM roofline: the method takes one exp(delta*A) per (b, t, d, n)
-    in each direction (2*N per element), and the SFUs deliver SFU_PER_CLK_PER_SM results per clock per SM."""
+def alu_co_bounds(wl, ms_fwd, ms_bwd, sms):
+    """The two arithmetic pipes' bounds beside the HBM roofline, from the method's own operation counts: one
+    exp(delta*A) per (b, t, d, n) in each direction, and FP32_OPS_PER_CELL multiply-adds per cell."""
     mhz = 2070.0
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             mhz = float(json.load(f).get("sm_max_mhz", mhz))
     except Exception:
         pass
-    exps = 2 * wl.B * wl.L * wl.D * wl.N
-    peak = SFU_PER_CLK_PER_SM * sms * mhz * 1e6
-    ach = exps / (ms * 1e-3)
-    return {"bound": "alu", "pipe": "MUFU ex2", "exps_per_step": exps, "achieved": ach, "peak": peak, "unit": "exp/s",
-            "frac": round(ach / peak, 4), "peak_from": f"{SFU_PER_CLK_PER_SM} per clock per SM x {sms} SMs x {mhz:.0f} MHz"}
+    cells = wl.B * wl.L * wl.D * wl.N
+    s = (ms_fwd + ms_bwd) * 1e-3
+    exps = 2 * cells
+    fma = cells * (FP32_OPS_PER_CELL["scan_fwd"] + FP32_OPS_PER_CELL["scan_bwd"])
+    pk_exp = SFU_PER_CLK_PER_SM * sms * mhz * 1e6
+    pk_fma = FMA_PER_CLK_PER_SM * sms * mhz * 1e6
+    return {
+        "mufu_ex2": {"per_step": exps, "achieved": exps / s, "peak": pk_exp, "unit": "exp/s",
+                     "frac": round(exps / s / pk_exp, 4), "floor_us": round(exps / pk_exp * 1e6, 1)},
+        "fp32_fma": {"per_step": fma, "achieved": fma / s, "peak": pk_fma, "unit": "op/s",
+                     "frac": round(fma / s / pk_fma, 4), "floor_us": round(fma / pk_fma * 1e6, 1)},
+        "peak_from": f"per clock per SM x {sms} SMs x {mhz:.0f} MHz",
+    }
 
 
 def measured_peak():
@@ -260,6 +292,57 @@ def run_reference(args, ws, rank):
 
 # ---------------------------------------------------------------- our arm
 
+def time_scan_workload(wl, dev, peak, iters=10, warmup=3):
+    """Scan forward and backward of one workload through the public API, each call bracketed by CUDA events on
+    the current stream (inputs resident in HBM, parameter gradients accumulating), with the algorithmic bytes."""
+    import numpy as np
+    import torch
+
+    import mamba_selective_ssm_gb300 as ss
+    from workloads import make_scan_inputs
+
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    inp = make_scan_inputs(wl, seed=0)
+    X = {k: torch.from_numpy(np.ascontiguousarray(v)).to(tdt if k not in ("A", "Dv") else torch.float32).to(dev)
+         for k, v in inp.items() if k in ("x", "delta", "z", "Bm", "Cm", "dy", "A", "Dv")}
+    del inp
+    st = torch.cuda.current_stream(dev)
+    f32 = dict(device=dev, dtype=torch.float32)
+    B, L, D, N = wl.B, wl.L, wl.D, wl.N
+    out = {"dx": torch.empty((B, L, D), **f32), "ddelta": torch.empty((B, L, D), **f32), "dz": torch.empty((B, L, D), **f32),
+           "dB": torch.empty((B, L, N), **f32), "dC": torch.empty((B, L, N), **f32), "dh0": torch.empty((B, D, N), **f32)}
+    dA, dD = torch.zeros((D, N), **f32), torch.zeros((D,), **f32)
+    wsz = max(ss.scan_bwd_workspace_size(B, L, D, N, wl.chunk, tdt), ss.scan_fwd_workspace_size(B, L, D, N, wl.chunk, tdt), 16)
+    W = torch.empty(wsz, device=dev, dtype=torch.uint8)
+    tf, tb = [], []
+    for i in range(warmup + iters):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(st)
+        y, ck, _ = ss.ss_scan_fwd(X["x"], X["delta"], X["A"], X["Bm"], X["Cm"], X["Dv"], X["z"], chunk=wl.chunk,
+                                  workspace=W)
+        e1.record(st)
+        ss.ss_scan_bwd(X["x"], X["delta"], X["A"], X["Bm"], X["Cm"], X["Dv"], X["z"], ck, X["dy"], chunk=wl.chunk,
+                       dA=dA, dD=dD, workspace=W, out=out)
+        e2.record(st)
+        if i >= warmup:
+            tf.append((e0, e1))
+            tb.append((e1, e2))
+    torch.cuda.synchronize(dev)
+    ms_f = statistics.median(a.elapsed_time(b) for a, b in tf)
+    ms_b = statistics.median(a.elapsed_time(b) for a, b in tb)
+    alg = algorithmic_bytes(wl)
+    ovh = checkpoint_overhead_bytes(wl, wl.chunk)
+    res = {"config": {"B": B, "L": L, "D": D, "N": N, "dtype": wl.dtype, "chunk": wl.chunk}}
+    for n, ms in (("scan_fwd", ms_f), ("scan_bwd", ms_b)):
+        gbs = alg[n] / (ms * 1e-3) / 1e9
+        res[n] = {"ms": round(ms, 5), "alg_bytes": alg[n], "overhead_bytes": ovh, "GB/s": round(gbs, 1),
+                  "frac": round(gbs / peak, 4)}
+    both = alg["scan_fwd"] + alg["scan_bwd"]
+    res["scan_fwd_bwd"] = {"ms": round(ms_f + ms_b, 5), "elems_per_s": B * L * D / ((ms_f + ms_b) * 1e-3),
+                           "frac": round(both / ((ms_f + ms_b) * 1e-3) / 1e9 / peak, 4)}
+    return res
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -384,22 +467,25 @@ def main():
     ms_step = ms_total / args.steps
     elems = B * L * D
     value = elems * ws / (ms_step * 1e-3)
-    alg = algorithmic_bytes(wl, chunk)
+    alg = algorithmic_bytes(wl)
+    ovh = checkpoint_overhead_bytes(wl, chunk)
     peak, peak_kind = measured_peak()
     kern = {}
     for n in names:
         gbs = alg[n] / (per_call[n] * 1e-3) / 1e9
         kern[n] = {"ms": round(per_call[n], 5), "alg_bytes": alg[n], "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        if n in ("scan_fwd", "scan_bwd"):
+            kern[n]["overhead_bytes"] = ovh
     dom = max(names, key=lambda n: per_call[n])
     traffic = profiled_traffic(dom, wl.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["GB/s"], "peak": peak, "unit": "GB/s",
                 "frac": kern[dom]["frac"], "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                "alg_bytes_per_launch": alg[dom]}
+                "alg_bytes_per_launch": alg[dom],
+                "alg_bytes_from": f"one checkpoint per {ALG_CHUNK} steps (after the first); the run's chunk-{chunk} "
+                                  "checkpoints are overhead_bytes",
+                "overhead_bytes": kern[dom].get("overhead_bytes", 0)}
     scan_ms = per_call["scan_fwd"] + per_call["scan_bwd"]
     scan_bytes = alg["scan_fwd"] + alg["scan_bwd"]
-    # the same two calls with one checkpoint per 256 steps (fewer checkpoint bytes, same other traffic)
-    alg256 = algorithmic_bytes(wl, 256)
-    scan_bytes_256 = alg256["scan_fwd"] + alg256["scan_bwd"]
 
     # ---- the producers and fusions next to the hot path, each timed alone on the same tensors (L2 flushed)
     nxt = {}
@@ -466,6 +552,14 @@ def main():
             ms = sum(a0.elapsed_time(a1) for a0, a1 in evp) / iters
             gbs = nbytes / (ms * 1e-3) / 1e9
             nxt[n] = {"ms": round(ms, 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+
+    # ---- the scan on the other workloads of the method (timed the same way, inputs resident in HBM)
+    others = {}
+    if not args.no_others and ws == 1:
+        for oname in ("long", "short", "mamba130m"):
+            if oname == wl.name:
+                continue
+            others[oname] = time_scan_workload(get_config(oname), dev, peak, iters=10)
 
     # ---- end to end through the public API: pinned host inputs in, results out, every step.
     # Three streams pipeline consecutive steps: step i's host->device copies (into one of two input slots)
@@ -544,8 +638,10 @@ def main():
             "scan_fwd_bwd": {"ms": round(scan_ms, 5), "elems_per_s": elems / (scan_ms * 1e-3),
                              "alg_GB/s": round(scan_bytes / (scan_ms * 1e-3) / 1e9, 1),
                              "frac": round(scan_bytes / (scan_ms * 1e-3) / 1e9 / peak, 4),
-                             "frac_at_chunk256_bytes": round(scan_bytes_256 / (scan_ms * 1e-3) / 1e9 / peak, 4),
-                             "exp_co_bound": exp_co_bound(wl, scan_ms, torch.cuda.get_device_properties(dev).multi_processor_count)},
+                             "alg_bytes": scan_bytes, "overhead_bytes": 2 * ovh,
+                             "alu_co_bounds": alu_co_bounds(wl, per_call["scan_fwd"], per_call["scan_bwd"],
+                                                            torch.cuda.get_device_properties(dev).multi_processor_count)},
+            "other_workloads": others or None,
             "kernels": kern, "next_kernels": nxt or None, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps,
         }), flush=True)

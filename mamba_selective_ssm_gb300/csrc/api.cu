@@ -51,8 +51,8 @@ extern "C" const char* ss_strerror(int code) {
     case SS_ERR_NULL: return "a required pointer is NULL";
     case SS_ERR_DIM: return "a size is non-positive or out of the supported range";
     case SS_ERR_UNSUPPORTED:
-      return "unsupported configuration (N must be 4, 8 or 16; dtype SS_F32 or SS_BF16; d_conv 1..4; chunk a multiple of 16 "
-             "within the backward's shared-memory budget)";
+      return "unsupported configuration (N must be 4, 8 or 16; dtype SS_F32 or SS_BF16; d_conv 1..4; chunk 8 or a multiple "
+             "of 16, at most 512 in the backward)";
     case SS_ERR_ALIGN: return "misaligned buffer (pointers must be 16-byte aligned; D and dim multiples of 8; bf16 with N=4 needs even L)";
     case SS_ERR_WORKSPACE: return "workspace missing or smaller than the *_workspace_size() query";
     case SS_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";

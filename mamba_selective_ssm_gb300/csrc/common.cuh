@@ -105,6 +105,16 @@ struct ActT<float> {
     reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
     reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
   }
+  // 2 consecutive elements (p 8-byte aligned) as a packed pair
+  __device__ __forceinline__ static float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+  // 4 consecutive elements (p 16-byte aligned) as two packed pairs
+  __device__ __forceinline__ static void ld4x2(const float* p, float2& a, float2& b) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    a = make_float2(v.x, v.y);
+    b = make_float2(v.z, v.w);
+  }
+  __device__ __forceinline__ static void st1(float* p, float v) { *p = v; }
+  __device__ __forceinline__ static void st2(float* p, float a, float b) { *reinterpret_cast<float2*>(p) = make_float2(a, b); }
 };
 
 template <>
@@ -129,6 +139,19 @@ struct ActT<__nv_bfloat16> {
   }
   __device__ __forceinline__ static void st8(__nv_bfloat16* p, const float* v) {
     *reinterpret_cast<uint4*>(p) = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+  }
+  __device__ __forceinline__ static float2 ld2(const __nv_bfloat16* p) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(bf16_lo(w), bf16_hi(w));
+  }
+  __device__ __forceinline__ static void ld4x2(const __nv_bfloat16* p, float2& a, float2& b) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    a = make_float2(bf16_lo(w.x), bf16_hi(w.x));
+    b = make_float2(bf16_lo(w.y), bf16_hi(w.y));
+  }
+  __device__ __forceinline__ static void st1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+  __device__ __forceinline__ static void st2(__nv_bfloat16* p, float a, float b) {
+    *reinterpret_cast<uint32_t*>(p) = pack2(a, b);
   }
 };
 

@@ -21,6 +21,11 @@
 // channel tile.  ss_bwd_reduce_kernel adds the partials of
 // dB/dC and of dA/dD in fixed order.  No atomics: results are bitwise
 // reproducible.
+// Sequence segments (few batch rows, long sequences): a summary kernel gives
+// each later segment's adjoint at its start from a zero carry and its sum of
+// delta; the warp-shuffle associative scan of scan_common.cuh composes them
+// into the carry arriving at the end of every segment, from which each
+// segment's CTAs run independently.
 #include "scan_common.cuh"
 
 namespace {
@@ -94,6 +99,7 @@ struct BwdParams {
   int P, Ls;      // sequence segments (P = 1: one CTA row walks whole batch rows)
   float* gsum;    // [B][P][D][N] adjoint a_tb G_tb at each segment's start from a zero carry at its end
   float* dsum;    // [B][P][D]    sum of delta over each segment
+  float* gin;     // [B][P][D][N] carry a G arriving at the end of each segment (combine kernel output)
   const float* dt_bias;  // fused discretisation: delta = f(raw + dt_bias), f = softplus if dsp
   int dsp;
   int fuse;              // dt_bias != NULL or dsp
@@ -390,24 +396,15 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
     const int kc = cur.kc, tl = cur.tl;
 
     if (cur.first) {  // entering batch row b: the gradient arriving on h_{te-1}
+      // (with segments, the combine kernel composed it from dh_last and the later segments' summaries)
+      const float* src = segs ? p.gin + ((size_t)b * p.P + sgm) * p.D * N
+                              : (p.dh_last ? p.dh_last + (size_t)b * p.D * N : nullptr);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.dh_last != nullptr && dvalid)
-          v = *reinterpret_cast<const float4*>(p.dh_last + ((size_t)b * p.D + dg + j) * N + n0);
+        if (src != nullptr && dvalid) v = *reinterpret_cast<const float4*>(src + (size_t)(dg + j) * N + n0);
         ga[j][0] = f2(v.x, v.y);
         ga[j][1] = f2(v.z, v.w);
-        // carry back through the later segments: ga <- exp2(A' sum(delta)) ga + ga_segment
-        if (segs && dvalid) {
-#pragma unroll 4
-          for (int s2 = p.P - 1; s2 > sgm; --s2) {
-            const size_t row = ((size_t)b * p.P + s2) * p.D + dg + j;
-            const float2 ds2 = bc2(p.dsum[row]);
-            const float4 gs = *reinterpret_cast<const float4*>(p.gsum + row * N + n0);
-            ga[j][0] = fma2(ex2_2(mul2(ds2, Ap[j][0])), ga[j][0], f2(gs.x, gs.y));
-            ga[j][1] = fma2(ex2_2(mul2(ds2, Ap[j][1])), ga[j][1], f2(gs.z, gs.w));
-          }
-        }
       }
     }
 
@@ -822,7 +819,7 @@ inline int bwd_seg_unit(int chunk) { return chunk > kTT ? chunk : kTT; }
 
 struct BwdPlan {
   int ndt, gy, pmax;
-  size_t off_dAD, off_gsum, off_dsum, total;
+  size_t off_dAD, off_gsum, off_dsum, off_gin, total;
 };
 
 inline BwdPlan make_plan(int B, int L, int D, int N, int chunk) {
@@ -836,8 +833,10 @@ inline BwdPlan make_plan(int B, int L, int D, int N, int chunk) {
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
   pl.off_dAD = up((size_t)pl.ndt * B * L * 2 * N * sizeof(float));
   pl.off_gsum = up(pl.off_dAD + (size_t)rows * D * (N + 2) * sizeof(float));
-  pl.off_dsum = up(pl.off_gsum + (pl.pmax > 1 ? (size_t)B * pl.pmax * D * N * sizeof(float) : 0));
-  pl.total = pl.off_dsum + (pl.pmax > 1 ? (size_t)B * pl.pmax * D * sizeof(float) : 0);
+  const size_t st = pl.pmax > 1 ? (size_t)B * pl.pmax * D * N * sizeof(float) : 0;
+  pl.off_dsum = up(pl.off_gsum + st);
+  pl.off_gin = up(pl.off_dsum + (pl.pmax > 1 ? (size_t)B * pl.pmax * D * sizeof(float) : 0));
+  pl.total = pl.off_gin + st;
   return pl;
 }
 
@@ -860,6 +859,7 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
   p.ws_dAD = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_dAD);
   p.gsum = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_gsum);
   p.dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_dsum);
+  p.gin = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_gin);
   p.tcols = p.chunk == kS ? 0u : tmem_cols(p.chunk);
   CUtensorMap tm[6];
   const uint64_t adims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
@@ -922,6 +922,8 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
   cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     skern<<<dim3(pl.ndt, p.B * (p.P - 1)), Geo<N, DT>::NT, smem_s, stream>>>(p, tm[0], tm[2], tm[3], tm[5]);
     if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+    if (seg_combine<true>(SegCombine{p.A, p.dsum, p.gsum, p.dh_last, p.gin, p.P, p.D, N}, p.B, stream) != cudaSuccess)
+      return SS_ERR_CUDA;
   }
   kern<<<dim3(pl.ndt, rows), Geo<N, DT>::NT, smem_launch, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4], tm[5]);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
@@ -987,8 +989,8 @@ extern "C" int ss_scan_bwd(const void* x, const void* delta, const float* A, con
   if (workspace == nullptr || ws_bytes < pl.total) return SS_ERR_WORKSPACE;
   if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
   BwdParams p{A, Dv, ckpt, dh_last, dx, ddelta, dz, dh0, nullptr, nullptr, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 0,
-              1, L, nullptr, nullptr, dt_bias, delta_softplus ? 1 : 0, (dt_bias != nullptr || delta_softplus) ? 1 : 0,
-              d_dt_bias};
+              1, L, nullptr, nullptr, nullptr, dt_bias, delta_softplus ? 1 : 0,
+              (dt_bias != nullptr || delta_softplus) ? 1 : 0, d_dt_bias};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool wide = bwd_channels(N, chunk) == 64;
   if (dtype == SS_F32) {

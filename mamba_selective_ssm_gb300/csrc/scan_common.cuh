@@ -43,9 +43,10 @@ struct Geo {
 // carry from the summaries of the segments before (forward) or after
 // (backward) it:  carry <- exp2(A log2e * sum(delta)) * carry + contribution.
 
-// Upper bound on P used to size the summary workspace: aims at ~2400 CTAs.
-inline int seg_pmax(long long ctas, int L, int unit) {
-  long long pm = (2432 + ctas - 1) / ctas;
+// Upper bound on P used to size the summary workspace: aims at about `target`
+// CTAs in all (16 per SM of 152 by default).
+inline int seg_pmax(long long ctas, int L, int unit, long long target = 2432) {
+  long long pm = (target + ctas - 1) / ctas;
   const long long units = (L + unit - 1) / unit;
   if (pm > 64) pm = 64;
   if (pm > units) pm = units;
@@ -93,6 +94,95 @@ __device__ __forceinline__ void delta_transform4(float* dv, const float* bias_s,
     if (softplus) v = softplus_f(v);
     dv[e] = (row_ok && e < d_left) ? v : 0.f;
   }
+}
+
+// Segment carries by a warp-shuffle associative scan.  Segment v maps the
+// carry entering it to the carry leaving it by c -> alpha_v c + beta_v, with
+// alpha_v = exp2(A log2e * sum of delta over v) and beta_v the segment's
+// summary (its contribution from a zero carry).  The maps are composed by an
+// inclusive scan of the affine pairs, (a1, b1) then (a2, b2) = (a1 a2,
+// a2 b1 + b2), and applied to `init` (NULL: zero).  Forward (REV = false):
+// segments run v = 0 .. P-1, summaries of 0 .. P-2 exist, out[v] is the state
+// entering v.  Backward (REV = true): the adjoint runs from the last segment
+// to the first, so v counts segments from the end (segment P-1-v), summaries of
+// segments 1 .. P-1 exist, and out[segment] is the carry arriving at its end.
+// CTA (32 x 8) = 32 consecutive (d, n) columns of one batch row (blockIdx.y):
+// the pairs pass through shared memory so that global accesses stay coalesced;
+// warp w scans columns w, w + 8, w + 16, w + 24 with lane l holding segments
+// 2l and 2l + 1 of the scan order (P <= kSegMax).
+constexpr int kSegMax = 64;
+
+struct SegCombine {
+  const float* A;     // [D, N]
+  const float* dsum;  // [B][P][D]    sum of delta over each segment
+  const float* summ;  // [B][P][D][N] each segment's contribution from a zero carry
+  const float* init;  // [B][D][N]    carry entering the scan (h0 or dh_last), or NULL
+  float* out;         // [B][P][D][N]
+  int P, D, N;
+};
+
+template <bool REV>
+__global__ void __launch_bounds__(256) seg_combine_kernel(const SegCombine c) {
+  __shared__ float al[kSegMax][33], be[kSegMax][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int b = blockIdx.y, P = c.P;
+  const long long DN = (long long)c.D * c.N;
+  const long long col = (long long)blockIdx.x * 32 + tx;
+  const bool ok = col < DN;
+  for (int v = ty; v < kSegMax; v += 8) {
+    float a = 1.f, bv = 0.f;  // identity map where the scan has no segment
+    if (ok && v < P - 1) {
+      const size_t row = (size_t)b * P + (REV ? P - 1 - v : v);
+      a = ex2(c.A[col] * kLog2e * c.dsum[row * c.D + col / c.N]);
+      bv = c.summ[row * DN + col];
+    }
+    al[v][tx] = a;
+    be[v][tx] = bv;
+  }
+  __syncthreads();
+  for (int k = ty; k < 32; k += 8) {
+    const long long cc = (long long)blockIdx.x * 32 + k;
+    const float a0 = al[2 * tx][k], b0 = be[2 * tx][k], a1 = al[2 * tx + 1][k], b1 = be[2 * tx + 1][k];
+    float Ac = a0 * a1, Bc = fmaf(a1, b0, b1);  // segment 2l, then 2l + 1
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float ap = __shfl_up_sync(0xffffffffu, Ac, off), bp = __shfl_up_sync(0xffffffffu, Bc, off);
+      if (tx >= off) {
+        Bc = fmaf(Ac, bp, Bc);
+        Ac *= ap;
+      }
+    }
+    float Ae = __shfl_up_sync(0xffffffffu, Ac, 1), Be = __shfl_up_sync(0xffffffffu, Bc, 1);
+    if (tx == 0) {
+      Ae = 1.f;
+      Be = 0.f;
+    }
+    const float c0 = (c.init != nullptr && cc < DN) ? c.init[(size_t)b * DN + cc] : 0.f;
+    const float in0 = fmaf(Ae, c0, Be);  // entering segment 2l of the scan order
+    __syncwarp();
+    al[2 * tx][k] = in0;
+    al[2 * tx + 1][k] = fmaf(a0, in0, b0);  // entering segment 2l + 1
+  }
+  __syncthreads();
+  for (int v = ty; v < P; v += 8)
+    if (ok) c.out[((size_t)b * P + (REV ? P - 1 - v : v)) * DN + col] = al[v][tx];
+}
+
+template <bool REV>
+inline cudaError_t seg_combine(const SegCombine& c, int B, cudaStream_t s) {
+  const long long DN = (long long)c.D * c.N;
+  seg_combine_kernel<REV><<<dim3((unsigned)((DN + 31) / 32), B), 256, 0, s>>>(c);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- lane reductions
+// Reduce-scatter step between lane and lane ^ mask, which each hold v0 and v1:
+// afterwards the lane with `hi` set holds the pair's sum of v1, the other lane
+// the pair's sum of v0.  Each lane adds in a fixed order (its own value first),
+// so the result does not depend on timing.
+__device__ __forceinline__ float rs_pair(float v0, float v1, bool hi, int mask) {
+  const float send = hi ? v0 : v1;
+  return (hi ? v1 : v0) + __shfl_xor_sync(0xffffffffu, send, mask);
 }
 
 }  // namespace ssk

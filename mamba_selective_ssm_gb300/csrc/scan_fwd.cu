@@ -2,18 +2,27 @@
 //
 //   h_t = exp(delta_t * A) * h_{t-1} + delta_t * B_t * x_t,   y_t = (C_t . h_t + D x_t) * silu(z_t)
 //
-// One CTA = 32 channels of one batch row; the sequence is walked once, in
-// order, 16 steps per TMA tile, with the N-state recurrences of every channel
-// held in registers (2 channels x 4 states per thread, f32x2-packed).  The
-// exponent uses one ex2 per (t, d, n) with A pre-scaled by log2 e.  Per tile:
-//   1. thread 0 waits (bounded) on the tile's mbarrier;
-//   2. all threads widen delta, delta*x, B_t, C_t to fp32 in shared memory;
-//   3. every thread advances its 8 recurrences over the 16 steps and the NG
-//      lanes of a channel pair reduce C_t . h_t across states;
-//   4. the tile epilogue forms y = (s + D x) * silu(z) with 16-byte stores;
-//   5. thread 0 re-arms the freed stage with the tile NST ahead.
+// Main kernel: one CTA = one warp = CG channels of one batch row (CG = 32 /
+// (N/4)).  Lane (ng, c) owns channel c and states 4ng .. 4ng+3: four (d, n)
+// recurrences in registers, f32x2-packed, with one ex2 per (t, d, n) (A
+// pre-scaled by log2 e).  The sequence is walked once, in order, in 16-step
+// tiles that TMA stages into a 4-deep ring.  The recurrence reads delta and x
+// straight from the staging slot; B_t and C_t, shared by every lane of a state
+// quad, are widened to fp32 once per tile so that each step loads them with
+// one 128-bit broadcast read.  C_t . h_t is summed over the N/4 lanes of a
+// channel by a shuffle reduce-scatter over four steps (two when N = 8), after
+// which every lane holds the complete sum of one (t, d) and forms
+// y = (s + D x) * silu(z) itself.  A warp needs no block barrier: copies are
+// observed on mbarriers and slot reuse is ordered by warp syncs, so the ~13
+// warps an SM holds on a Mamba-sized layer never wait on one another.
 // The state entering step c*chunk is stored as checkpoint c ([B, chunks, D, N])
 // for the backward.
+//
+// Sequence segments (few batch rows, long sequences): a summary kernel gives
+// each segment's zero-start end state and its sum of delta; a combine kernel
+// composes the segments' affine maps h -> exp2(A' sum delta) h + end state
+// with a warp-shuffle associative scan and writes the state entering every
+// segment; the main kernel then runs each segment from its carry.
 #include "scan_common.cuh"
 
 namespace {
@@ -23,38 +32,6 @@ using namespace ssk;
 __device__ unsigned g_fwd_err;
 
 constexpr int kNST = 4;  // TMA pipeline depth (tiles in flight)
-
-// Forward geometry: CPT channels x 4 states per thread (CPT = 1 doubles the
-// warps per SM relative to the backward's 2 x 4 cells, which the forward can
-// afford because it keeps no per-step history).
-template <int N, int CPT, int DT>
-struct GeoF {
-  static constexpr int NG = N / 4;
-  static constexpr int CG = 32 / NG;
-  static constexpr int WC = CPT * CG;
-  static constexpr int W = DT / WC;
-  static constexpr int NT = 32 * W;
-  static_assert(W >= 1 && DT % WC == 0, "a CTA holds whole warps");
-};
-
-constexpr int kFDT = 32;  // channels per forward CTA
-
-template <typename T, int N, int DT>
-struct FwdSmem {
-  alignas(128) T dlt[kNST][kTT * DT];
-  alignas(128) T x[kNST][kTT * DT];
-  alignas(128) T z[kNST][kTT * DT];
-  alignas(128) T Bm[kNST][kTT * N];
-  alignas(128) T Cm[kNST][kTT * N];
-  alignas(16) float dlt_f[kTT * DT];
-  alignas(16) float dx_f[kTT * DT];
-  alignas(16) float B_f[kTT * N];
-  alignas(16) float C_f[kTT * N];
-  alignas(16) float yp[kTT][N / 4][DT + 8];  // per-lane shares of C_t . h_t over the lane's 4 states (row pitch spreads banks)
-  alignas(16) float Dv_s[DT];
-  alignas(16) float bias_s[DT];  // dt_bias of the fused discretisation (0 without one)
-  alignas(8) uint64_t full[kNST];
-};
 
 struct FwdParams {
   const float* A;
@@ -67,197 +44,89 @@ struct FwdParams {
   int P, Ls;     // sequence segments (P = 1: one CTA row walks whole batch rows)
   float* hsum;   // [B][P][D][N] state at the end of each segment from a zero start
   float* dsum;   // [B][P][D]    sum of delta over each segment
+  float* hin;    // [B][P][D][N] state entering each segment (combine kernel output)
   const float* dt_bias;  // fused discretisation: delta = f(raw + dt_bias), f = softplus if dsp
   int dsp;
   int fuse;              // dt_bias != NULL or dsp
 };
 
-template <typename T, int N, int DT>
-struct FwdSumSmem {
+// Main-kernel geometry: one warp per CTA, one channel x 4 states per lane, CG = 32 / (N/4) channels.
+template <int N>
+struct GeoW {
+  static constexpr int NG = N / 4;
+  static constexpr int CG = 32 / NG;
+  static constexpr int DT = CG;
+};
+
+template <typename T, int N>
+struct FwdSmem {
+  static constexpr int DT = GeoW<N>::DT;
   alignas(128) T dlt[kNST][kTT * DT];
   alignas(128) T x[kNST][kTT * DT];
+  alignas(128) T z[kNST][kTT * DT];
   alignas(128) T Bm[kNST][kTT * N];
-  alignas(16) float dlt_f[kTT * DT];
-  alignas(16) float dx_f[kTT * DT];
-  alignas(16) float B_f[kTT * N];
+  alignas(128) T Cm[kNST][kTT * N];
+  alignas(16) float dlt_f[kTT * DT];  // fused discretisation only: the tile's transformed delta
+  alignas(16) float B_f[kTT * N];     // the tile's B_t, C_t in fp32
+  alignas(16) float C_f[kTT * N];
   alignas(16) float bias_s[DT];
   alignas(8) uint64_t full[kNST];
 };
 
-// Segment summaries for segments 0 .. P-2: the state each reaches from a zero
-// start, and its sum of delta.  CTA = (channel tile, (batch row, segment)).
-template <int N, typename T, int CPT, int DT, bool FUSE>
-__global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_summary_kernel(const FwdParams p,
-                                                                      const __grid_constant__ CUtensorMap tm_dlt,
-                                                                      const __grid_constant__ CUtensorMap tm_x,
-                                                                      const __grid_constant__ CUtensorMap tm_B) {
-  using G = GeoF<N, CPT, DT>;
+// SUM = true: the segment-summary pass.  CTA row y = (batch row, segment) for
+// segments 0 .. P-2, which are whole tiles; only delta, x and B_t are read and
+// the kernel writes the segment's end state from a zero start and its sum of delta.
+template <int N, typename T, bool FUSE, bool SUM>
+__global__ void __launch_bounds__(32) scan_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
+                                                       const __grid_constant__ CUtensorMap tm_x,
+                                                       const __grid_constant__ CUtensorMap tm_z,
+                                                       const __grid_constant__ CUtensorMap tm_B,
+                                                       const __grid_constant__ CUtensorMap tm_C) {
+  using G = GeoW<N>;
   using AT = ActT<T>;
+  constexpr int NG = G::NG, CG = G::CG, DT = G::DT;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  FwdSumSmem<T, N, DT>& S = *reinterpret_cast<FwdSumSmem<T, N, DT>*>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ng = lane / G::CG, cg = lane % G::CG;
-  const int dl = warp * G::WC + cg * CPT;
+  FwdSmem<T, N>& S = *reinterpret_cast<FwdSmem<T, N>*>(smem_raw);
+
+  const int lane = threadIdx.x;
+  const int ng = lane / CG, c = lane % CG;
+  const int n0 = ng * 4;
   const int d0 = blockIdx.x * DT;
-  const int dg = d0 + dl;
+  const int dg = d0 + c;
   const bool dvalid = dg < p.D;
-  const int n0 = ng * 4;
-  const int b = (int)blockIdx.y / (p.P - 1), sgm = (int)blockIdx.y % (p.P - 1);
-  const int tb = sgm * p.Ls;
-  const int nitems = p.Ls / kTT;  // segments before the last are whole
-  constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
-  constexpr uint32_t kStageBytes = 2 * kActBytes + kTT * N * AT::kBytes;
-  float2 Ap[CPT][2];
-#pragma unroll
-  for (int j = 0; j < CPT; ++j)
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const float* a = p.A + (size_t)(dvalid ? dg + j : 0) * N + n0 + 2 * q;
-      Ap[j][q] = dvalid ? f2(a[0] * kLog2e, a[1] * kLog2e) : f2(0.f, 0.f);
-    }
-  auto issue = [&](int k) {
-    fence_proxy_async_smem();  // the slot's earlier readers passed a barrier before this call
-    const int slot = k % kNST, t0 = tb + k * kTT;
-    mbar_arrive_expect_tx(&S.full[slot], kStageBytes);
-    tma_load_3d(S.dlt[slot], &tm_dlt, &S.full[slot], d0, t0, b);
-    tma_load_3d(S.x[slot], &tm_x, &S.full[slot], d0, t0, b);
-    tma_load_2d(S.Bm[slot], &tm_B, &S.full[slot], t0 * N, b);
-  };
-  for (int c = tid; c < DT; c += G::NT) S.bias_s[c] = (p.dt_bias != nullptr && d0 + c < p.D) ? p.dt_bias[d0 + c] : 0.f;
-  if (tid == 0) {
-    prefetch_tmap(&tm_dlt); prefetch_tmap(&tm_x); prefetch_tmap(&tm_B);
-    for (int st = 0; st < kNST; ++st) mbar_init(&S.full[st], 1);
-    fence_barrier_init();
-    for (int k = 0; k < kNST && k < nitems; ++k) issue(k);
-  }
-  __syncthreads();
-  float2 h[CPT][2];
-  float dsum[CPT];
-#pragma unroll
-  for (int j = 0; j < CPT; ++j) {
-    h[j][0] = h[j][1] = f2(0.f, 0.f);
-    dsum[j] = 0.f;
-  }
-  for (int k = 0; k < nitems; ++k) {
-    const int slot = k % kNST;
-    bool ok = true;
-    if (tid == 0) ok = mbar_wait_bounded(&S.full[slot], (k / kNST) & 1, kWaitLimitNs);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
-        atomicOr(&g_fwd_err, kErrTmaTimeout);
-        for (int k2 = k; k2 < k + kNST && k2 < nitems; ++k2)
-          mbar_wait_bounded(&S.full[k2 % kNST], (k2 / kNST) & 1, 100000000ull);
-      }
-      return;
-    }
-    for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
-      float dv[4], xv[4];
-      AT::ld4(&S.dlt[slot][gi * 4], dv);
-      AT::ld4(&S.x[slot][gi * 4], xv);
-      if constexpr (FUSE) {
-        const int c4 = (gi % (DT / 4)) * 4;
-        delta_transform4(dv, S.bias_s, c4, tb + k * kTT + gi / (DT / 4) < p.L, p.D - d0 - c4, p.dsp);
-      }
-      reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
-      reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(dv[0] * xv[0], dv[1] * xv[1], dv[2] * xv[2], dv[3] * xv[3]);
-    }
-    for (int gi = tid; gi < kTT * N / 4; gi += G::NT) {
-      float bv[4];
-      AT::ld4(&S.Bm[slot][gi * 4], bv);
-      reinterpret_cast<float4*>(S.B_f)[gi] = make_float4(bv[0], bv[1], bv[2], bv[3]);
-    }
-    __syncthreads();
-    if (tid == 0 && k + kNST < nitems) issue(k + kNST);  // the slot is widened: refill it
-#pragma unroll
-    for (int r = 0; r < kTT; ++r) {
-      const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
-      const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
-#pragma unroll
-      for (int j = 0; j < CPT; ++j) {
-        const float dd = S.dlt_f[r * DT + dl + j];
-        const float2 dj = bc2(dd), xj = bc2(S.dx_f[r * DT + dl + j]);
-        dsum[j] += dd;
-        h[j][0] = fma2(ex2_2(mul2(dj, Ap[j][0])), h[j][0], mul2(xj, B01));
-        h[j][1] = fma2(ex2_2(mul2(dj, Ap[j][1])), h[j][1], mul2(xj, B23));
-      }
-    }
-    __syncthreads();
-  }
-  if (dvalid) {
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-      const size_t row = ((size_t)b * p.P + sgm) * p.D + dg + j;
-      *reinterpret_cast<float4*>(p.hsum + row * N + n0) = make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
-      if (ng == 0) p.dsum[row] = dsum[j];
-    }
-  }
-}
-
-template <int N, typename T, int CPT, int DT, bool FUSE>
-__global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_dlt,
-                                                              const __grid_constant__ CUtensorMap tm_x,
-                                                              const __grid_constant__ CUtensorMap tm_z,
-                                                              const __grid_constant__ CUtensorMap tm_B,
-                                                              const __grid_constant__ CUtensorMap tm_C) {
-  using G = GeoF<N, CPT, DT>;
-  using AT = ActT<T>;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  FwdSmem<T, N, DT>& S = *reinterpret_cast<FwdSmem<T, N, DT>*>(smem_raw);
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ng = lane / G::CG, cg = lane % G::CG;
-  const int dl = warp * G::WC + cg * CPT;  // first of the thread's channels, CTA-local
-  const int d0 = blockIdx.x * DT;
-  const int dg = d0 + dl;
-  const bool dvalid = dg < p.D;  // D is a multiple of 8, so dg+CPT-1 < D as well
-  const int n0 = ng * 4;
   const int L = p.L;
-  // P = 1: CTA row y walks batch rows y, y + gridDim.y, ... whole.
-  // P > 1: CTA row y owns one segment [tb, te) of batch row y / P.
-  const bool segs = p.P > 1;
-  const int sgm = segs ? (int)blockIdx.y % p.P : 0;
+  const bool segs = SUM || p.P > 1;
+  const int sgm = SUM ? (int)blockIdx.y % (p.P - 1) : segs ? (int)blockIdx.y % p.P : 0;
   const int tb = sgm * p.Ls;
   const int te = segs ? min(L, tb + p.Ls) : L;
   const int ntiles = (te - tb + kTT - 1) / kTT;
-  const int nb = segs ? 1 : (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;  // batch rows of this CTA
+  const int nb = segs ? 1 : (p.B - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
   const int nitems = nb * ntiles;
-  const int b_first = segs ? (int)blockIdx.y / p.P : (int)blockIdx.y;
-  // items (batch row, tile) in order; two cursors (consumer, TMA issuer) step
-  // through them without divisions
+  const int b_first = SUM ? (int)blockIdx.y / (p.P - 1) : segs ? (int)blockIdx.y / p.P : (int)blockIdx.y;
   struct Cursor {
     int b, ti;
   };
-  auto advance = [&](Cursor& c) {
-    if (++c.ti == ntiles) {
-      c.ti = 0;
-      c.b += (int)gridDim.y;
+  auto advance = [&](Cursor& cu) {
+    if (++cu.ti == ntiles) {
+      cu.ti = 0;
+      cu.b += (int)gridDim.y;
     }
   };
   Cursor icur{b_first, 0};
-  constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
-  constexpr uint32_t kBCBytes = kTT * N * AT::kBytes;
-  constexpr uint32_t kStageBytes = 3 * kActBytes + 2 * kBCBytes;
+  constexpr uint32_t kStageBytes = (SUM ? 2 : 3) * kTT * DT * AT::kBytes + (SUM ? 1 : 2) * kTT * N * AT::kBytes;
 
-  // exponent scale A * log2(e) of the thread's CPT x 4 cells
-  float2 Ap[CPT][2];
+  float2 Ap[2];
 #pragma unroll
-  for (int j = 0; j < CPT; ++j)
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      if (dvalid) {
-        const float* a = p.A + (size_t)(dg + j) * N + n0 + 2 * q;
-        Ap[j][q] = f2(a[0] * kLog2e, a[1] * kLog2e);
-      } else {
-        Ap[j][q] = f2(0.f, 0.f);
-      }
-    }
-  for (int c = tid; c < DT; c += G::NT) {
-    S.Dv_s[c] = (d0 + c < p.D) ? p.Dv[d0 + c] : 0.f;
-    S.bias_s[c] = (p.dt_bias != nullptr && d0 + c < p.D) ? p.dt_bias[d0 + c] : 0.f;
+  for (int q = 0; q < 2; ++q) {
+    const float* a = p.A + (size_t)(dvalid ? dg : 0) * N + n0 + 2 * q;
+    Ap[q] = dvalid ? f2(a[0] * kLog2e, a[1] * kLog2e) : f2(0.f, 0.f);
   }
+  const float Dc = dvalid ? p.Dv[dg] : 0.f;
+  if constexpr (FUSE)
+    for (int i = lane; i < DT; i += 32) S.bias_s[i] = (p.dt_bias != nullptr && d0 + i < p.D) ? p.dt_bias[d0 + i] : 0.f;
 
-  auto issue = [&](int k) {  // k: the item icur points at
-    fence_proxy_async_smem();  // the slot's earlier readers passed a barrier before this call
+  auto issue = [&](int k) {
+    fence_proxy_async_smem();
     const int slot = k % kNST;
     const int bb = icur.b;
     const int t0 = tb + icur.ti * kTT;
@@ -265,191 +134,167 @@ __global__ void __launch_bounds__(GeoF<N, CPT, DT>::NT) scan_fwd_kernel(const Fw
     mbar_arrive_expect_tx(&S.full[slot], kStageBytes);
     tma_load_3d(S.dlt[slot], &tm_dlt, &S.full[slot], d0, t0, bb);
     tma_load_3d(S.x[slot], &tm_x, &S.full[slot], d0, t0, bb);
-    tma_load_3d(S.z[slot], &tm_z, &S.full[slot], d0, t0, bb);
     tma_load_2d(S.Bm[slot], &tm_B, &S.full[slot], t0 * N, bb);
-    tma_load_2d(S.Cm[slot], &tm_C, &S.full[slot], t0 * N, bb);
+    if constexpr (!SUM) {
+      tma_load_3d(S.z[slot], &tm_z, &S.full[slot], d0, t0, bb);
+      tma_load_2d(S.Cm[slot], &tm_C, &S.full[slot], t0 * N, bb);
+    }
   };
-
-  if (tid == 0) {
+  if (lane == 0) {
     prefetch_tmap(&tm_dlt); prefetch_tmap(&tm_x); prefetch_tmap(&tm_z); prefetch_tmap(&tm_B); prefetch_tmap(&tm_C);
     for (int s = 0; s < kNST; ++s) mbar_init(&S.full[s], 1);
     fence_barrier_init();
     for (int k = 0; k < kNST && k < nitems; ++k) issue(k);
   }
-  __syncthreads();
+  __syncwarp();
 
-  float2 h[CPT][2];
+  // y at step r of the tile for this lane's channel, from its sum over n
+  auto finish1 = [&](int slot, int b, int t0, int r, float sv) {
+    const float xv = AT::ld(&S.x[slot][r * DT + c]);
+    const float zv = AT::ld(&S.z[slot][r * DT + c]);
+    const float o = fmaf(Dc, xv, sv) * zv * sigmoid(zv);
+    if (t0 + r < L && dvalid) AT::st1(reinterpret_cast<T*>(p.y) + ((size_t)b * L + t0 + r) * p.D + dg, o);
+  };
+
+  float2 h0, h1;
+  float dsum = 0.f;  // SUM: the segment's sum of delta
   Cursor cur{b_first, 0};
-  int tck = 0;  // t0 mod chunk (chunk > 8)
+  int tck = 0;
   for (int k = 0; k < nitems; ++k, advance(cur)) {
     const int slot = k % kNST;
     const int b = cur.b;
     const int ti = cur.ti;
     const int t0 = tb + ti * kTT;
-    if (ti == 0) tck = tb % p.chunk;
-
-    if (ti == 0) {  // entering batch row b: initial state
-#pragma unroll
-      for (int j = 0; j < CPT; ++j) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.h0 != nullptr && dvalid) v = *reinterpret_cast<const float4*>(p.h0 + ((size_t)b * p.D + dg + j) * N + n0);
-        h[j][0] = f2(v.x, v.y);
-        h[j][1] = f2(v.z, v.w);
-        // carry through the earlier segments: h <- exp2(A' sum(delta)) h + h_segment
-        if (dvalid) {
-#pragma unroll 4
-          for (int s2 = 0; s2 < sgm; ++s2) {
-            const size_t row = ((size_t)b * p.P + s2) * p.D + dg + j;
-            const float2 ds2 = bc2(p.dsum[row]);
-            const float4 hs = *reinterpret_cast<const float4*>(p.hsum + row * N + n0);
-            h[j][0] = fma2(ex2_2(mul2(ds2, Ap[j][0])), h[j][0], f2(hs.x, hs.y));
-            h[j][1] = fma2(ex2_2(mul2(ds2, Ap[j][1])), h[j][1], f2(hs.z, hs.w));
-          }
-        }
-      }
+    if (ti == 0) {
+      tck = tb % p.chunk;
+      const float* src = SUM ? nullptr
+                             : segs ? p.hin + ((size_t)b * p.P + sgm) * p.D * N : (p.h0 ? p.h0 + (size_t)b * p.D * N : nullptr);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (src != nullptr && dvalid) v = *reinterpret_cast<const float4*>(src + (size_t)dg * N + n0);
+      h0 = f2(v.x, v.y);
+      h1 = f2(v.z, v.w);
     }
-
-    bool ok = true;
-    if (tid == 0) ok = mbar_wait_bounded(&S.full[slot], (k / kNST) & 1, kWaitLimitNs);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
+    const bool ok = mbar_wait_bounded(&S.full[slot], (k / kNST) & 1, kWaitLimitNs);
+    if (__any_sync(0xffffffffu, !ok)) {
+      if (lane == 0) {
         atomicOr(&g_fwd_err, kErrTmaTimeout);
-        // copies in flight: items k .. k+kNST-1 before the first refill, k .. k+kNST-2 after it
-        const int kend = k + kNST - (k >= 1 ? 1 : 0);
-        for (int k2 = k; k2 < kend && k2 < nitems; ++k2)
+        for (int k2 = k; k2 < k + kNST && k2 < nitems; ++k2)
           mbar_wait_bounded(&S.full[k2 % kNST], (k2 / kNST) & 1, 100000000ull);
       }
       return;
     }
-    // every thread is past the previous tile's epilogue: its staging slot can be refilled
-    if (tid == 0 && k >= 1 && k - 1 + kNST < nitems) issue(k - 1 + kNST);
-
-    // widen the tile to fp32: delta, delta*x, B, C
-    for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
-      float dv[4], xv[4];
-      AT::ld4(&S.dlt[slot][gi * 4], dv);
-      AT::ld4(&S.x[slot][gi * 4], xv);
-      if constexpr (FUSE) {
+    if constexpr (FUSE) {
+      for (int gi = lane; gi < kTT * DT / 4; gi += 32) {
+        float dv[4];
+        AT::ld4(&S.dlt[slot][gi * 4], dv);
         const int c4 = (gi % (DT / 4)) * 4;
         delta_transform4(dv, S.bias_s, c4, t0 + gi / (DT / 4) < L, p.D - d0 - c4, p.dsp);
+        *reinterpret_cast<float4*>(&S.dlt_f[gi * 4]) = make_float4(dv[0], dv[1], dv[2], dv[3]);
       }
-      reinterpret_cast<float4*>(S.dlt_f)[gi] = make_float4(dv[0], dv[1], dv[2], dv[3]);
-      reinterpret_cast<float4*>(S.dx_f)[gi] = make_float4(dv[0] * xv[0], dv[1] * xv[1], dv[2] * xv[2], dv[3] * xv[3]);
     }
-    for (int gi = tid; gi < kTT * N / 4; gi += G::NT) {
-      float bv[4], cv[4];
+    for (int gi = lane; gi < kTT * N / 4; gi += 32) {
+      float bv[4];
       AT::ld4(&S.Bm[slot][gi * 4], bv);
-      AT::ld4(&S.Cm[slot][gi * 4], cv);
       reinterpret_cast<float4*>(S.B_f)[gi] = make_float4(bv[0], bv[1], bv[2], bv[3]);
-      reinterpret_cast<float4*>(S.C_f)[gi] = make_float4(cv[0], cv[1], cv[2], cv[3]);
-    }
-    __syncthreads();
-
-    // the recurrence over the tile's 16 steps (steps past L were zero-filled
-    // by TMA: delta = 0 gives a = 1 and no input, so they leave h unchanged)
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      constexpr int kH = kTT / 2;
-      // checkpoint: the state entering step t0 + 8 half (chunk is 8 or a multiple of the tile)
-      const int tc = t0 + half * kH;
-      if (dvalid && tc < L && (p.chunk == kS || (half == 0 && tck == 0))) {
-        const int c = p.chunk == kS ? tc / kS : tc / p.chunk;
-#pragma unroll
-        for (int j = 0; j < CPT; ++j)
-          *reinterpret_cast<float4*>(p.ckpt + (((size_t)b * p.nchunks + c) * p.D + dg + j) * N + n0) =
-              make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
-      }
-      float2 av[kH][CPT][2];
-#pragma unroll
-      for (int i = 0; i < kH; ++i) {  // exponentials first: independent of the state
-        const int r = half * kH + i;
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-          const float2 dj = bc2(S.dlt_f[r * DT + dl + j]);
-          av[i][j][0] = ex2_2(mul2(dj, Ap[j][0]));
-          av[i][j][1] = ex2_2(mul2(dj, Ap[j][1]));
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kH; ++i) {
-        const int r = half * kH + i;
-        const float4 Bv = *reinterpret_cast<const float4*>(&S.B_f[r * N + n0]);
-        const float4 Cv = *reinterpret_cast<const float4*>(&S.C_f[r * N + n0]);
-        const float2 B01 = f2(Bv.x, Bv.y), B23 = f2(Bv.z, Bv.w);
-        const float2 C01 = f2(Cv.x, Cv.y), C23 = f2(Cv.z, Cv.w);
-        float yj[CPT];
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-          const float2 xj = bc2(S.dx_f[r * DT + dl + j]);
-          h[j][0] = fma2(av[i][j][0], h[j][0], mul2(xj, B01));
-          h[j][1] = fma2(av[i][j][1], h[j][1], mul2(xj, B23));
-          const float2 yy = fma2(C23, h[j][1], mul2(C01, h[j][0]));
-          yj[j] = yy.x + yy.y;
-        }
-        // this lane's share of C_t . h_t; the NG shares are summed in the epilogue
-        if constexpr (CPT == 2) *reinterpret_cast<float2*>(&S.yp[r][ng][dl]) = f2(yj[0], yj[CPT - 1]);
-        else S.yp[r][ng][dl] = yj[0];
+      if constexpr (!SUM) {
+        float cv[4];
+        AT::ld4(&S.Cm[slot][gi * 4], cv);
+        reinterpret_cast<float4*>(S.C_f)[gi] = make_float4(cv[0], cv[1], cv[2], cv[3]);
       }
     }
-    __syncthreads();
-
-    // epilogue: y = (s + D x) * silu(z), four channels per thread
-    for (int gi = tid; gi < kTT * DT / 4; gi += G::NT) {
-      const int r = gi / (DT / 4), c4 = (gi % (DT / 4)) * 4;
-      const int t = t0 + r, d = d0 + c4;
-      if (t < L && d < p.D) {
-        float xv[4], zv[4];
-        AT::ld4(&S.x[slot][r * DT + c4], xv);
-        AT::ld4(&S.z[slot][r * DT + c4], zv);
-        float4 sv = *reinterpret_cast<const float4*>(&S.yp[r][0][c4]);
+    __syncwarp();
 #pragma unroll
-        for (int g = 1; g < N / 4; ++g) {
-          const float4 u = *reinterpret_cast<const float4*>(&S.yp[r][g][c4]);
-          sv.x += u.x; sv.y += u.y; sv.z += u.z; sv.w += u.w;
+    for (int rq = 0; rq < kTT; rq += 4) {
+      float ys[4];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int r = rq + s;
+        if (!SUM && (r == 0 || r == kS)) {
+          const int tc = t0 + r;
+          if (dvalid && tc < L && (p.chunk == kS || (r == 0 && tck == 0))) {
+            const int ci = p.chunk == kS ? tc / kS : tc / p.chunk;
+            *reinterpret_cast<float4*>(p.ckpt + (((size_t)b * p.nchunks + ci) * p.D + dg) * N + n0) =
+                make_float4(h0.x, h0.y, h1.x, h1.y);
+          }
         }
-        const float4 Dd = *reinterpret_cast<const float4*>(&S.Dv_s[c4]);
-        const float s0 = fmaf(Dd.x, xv[0], sv.x), s1 = fmaf(Dd.y, xv[1], sv.y);
-        const float s2 = fmaf(Dd.z, xv[2], sv.z), s3 = fmaf(Dd.w, xv[3], sv.w);
-        T* out = reinterpret_cast<T*>(p.y) + ((size_t)b * L + t) * p.D + d;
-        const float o0 = s0 * zv[0] * sigmoid(zv[0]), o1 = s1 * zv[1] * sigmoid(zv[1]);
-        const float o2 = s2 * zv[2] * sigmoid(zv[2]), o3 = s3 * zv[3] * sigmoid(zv[3]);
-        if constexpr (sizeof(T) == 4) {
-          *reinterpret_cast<float4*>(out) = make_float4(o0, o1, o2, o3);
-        } else {
-          *reinterpret_cast<uint2*>(out) = make_uint2(ActT<__nv_bfloat16>::pack2(o0, o1), ActT<__nv_bfloat16>::pack2(o2, o3));
+        float dv;
+        if constexpr (FUSE) dv = S.dlt_f[r * DT + c];
+        else dv = AT::ld(&S.dlt[slot][r * DT + c]);
+        const float uv = dv * AT::ld(&S.x[slot][r * DT + c]);
+        float2 B01, B23;
+        ActT<float>::ld4x2(&S.B_f[r * N + n0], B01, B23);
+        const float2 d2 = bc2(dv), u2 = bc2(uv);
+        h0 = fma2(ex2_2(mul2(d2, Ap[0])), h0, mul2(u2, B01));
+        h1 = fma2(ex2_2(mul2(d2, Ap[1])), h1, mul2(u2, B23));
+        if constexpr (SUM) {
+          dsum += dv;
+          continue;
+        }
+        float2 C01, C23;
+        ActT<float>::ld4x2(&S.C_f[r * N + n0], C01, C23);
+        const float2 yy = fma2(C23, h1, mul2(C01, h0));
+        ys[s] = yy.x + yy.y;
+        if constexpr (NG == 1) {
+          finish1(slot, b, t0, r, ys[s]);
+        } else if constexpr (NG == 2) {
+          if (s & 1) finish1(slot, b, t0, r - 1 + (ng & 1), rs_pair(ys[s - 1], ys[s], ng & 1, CG));
         }
       }
+      if constexpr (NG == 4 && !SUM) {  // the four steps: keep steps {2 b1, 2 b1 + 1}, then step ng
+        const bool b1 = (ng >> 1) & 1, b0 = ng & 1;
+        const float k0 = rs_pair(ys[0], ys[2], b1, 2 * CG);
+        const float k1 = rs_pair(ys[1], ys[3], b1, 2 * CG);
+        finish1(slot, b, t0, rq + ng, rs_pair(k0, k1, b0, CG));
+      }
     }
-    // no barrier here: the next tile's prologue writes only buffers this epilogue does not read,
-    // and its first barrier orders this epilogue before the next writes of yp and of the slot
     tck += kTT;
     if (tck >= p.chunk) tck -= p.chunk;
-
-    if (ti == ntiles - 1 && te == L && p.h_last != nullptr && dvalid) {
-#pragma unroll
-      for (int j = 0; j < CPT; ++j)
-        *reinterpret_cast<float4*>(p.h_last + ((size_t)b * p.D + dg + j) * N + n0) =
-            make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
-    }
+    __syncwarp();
+    if (lane == 0 && k + kNST < nitems) issue(k + kNST);
+    if (!SUM && ti == ntiles - 1 && te == L && p.h_last != nullptr && dvalid)
+      *reinterpret_cast<float4*>(p.h_last + ((size_t)b * p.D + dg) * N + n0) = make_float4(h0.x, h0.y, h1.x, h1.y);
+  }
+  if (SUM && dvalid) {
+    const size_t row = ((size_t)b_first * p.P + sgm) * p.D + dg;
+    *reinterpret_cast<float4*>(p.hsum + row * N + n0) = make_float4(h0.x, h0.y, h1.x, h1.y);
+    if (ng == 0) p.dsum[row] = dsum;
   }
 }
 
+// Segments only when the (batch row, channel tile) warps would leave the GPU
+// with fewer than four per SM.
 template <int N>
 int fwd_pmax(int B, int L, int D) {
-  const long long ctas = (long long)((D + kFDT - 1) / kFDT) * B;
-  return ctas >= 608 ? 1 : seg_pmax(ctas, L, kTT);
+  constexpr int DT = GeoW<N>::DT;
+  const long long warps = (long long)((D + DT - 1) / DT) * B;
+  return warps >= 608 ? 1 : seg_pmax(warps, L, kTT, 32 * 152);  // one-warp CTAs: aim at 32 per SM
+}
+
+struct FwdWs {
+  size_t off_dsum, off_hin, total;
+};
+
+inline FwdWs fwd_ws_layout(int B, int D, int N, int pm) {
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  const size_t st = (size_t)B * pm * D * N * sizeof(float);
+  FwdWs w;
+  w.off_dsum = up(st);
+  w.off_hin = up(w.off_dsum + (size_t)B * pm * D * sizeof(float));
+  w.total = w.off_hin + st;
+  return w;
 }
 
 size_t fwd_ws_bytes(int B, int L, int D, int N) {
   const int pm = N == 4 ? fwd_pmax<4>(B, L, D) : N == 8 ? fwd_pmax<8>(B, L, D) : fwd_pmax<16>(B, L, D);
   if (pm <= 1) return 0;
-  return (((size_t)B * pm * D * N * sizeof(float) + 255) & ~(size_t)255) + (size_t)B * pm * D * sizeof(float);
+  return fwd_ws_layout(B, D, N, pm).total;
 }
 
-template <int N, typename T, bool FUSE, int CPT = 1, int DT = kFDT>
+template <int N, typename T, bool FUSE>
 int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, void* ws,
                cudaStream_t stream) {
   constexpr int e = ActT<T>::kBytes;
+  constexpr int DT = GeoW<N>::DT;
   CUtensorMap tm[5];
   const uint64_t adims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
   const uint64_t astr[2] = {(uint64_t)p.D * e, (uint64_t)p.L * p.D * e};
@@ -464,19 +309,16 @@ int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, co
       !ssh::encode_tiled(&tm[4], ActT<T>::kTma, 2, Cm, bdims, bstr, bbox))
     return SS_ERR_CUDA;
   const int ndt = (p.D + DT - 1) / DT;
-  const size_t smem = sizeof(FwdSmem<T, N, DT>);
-  auto kern = scan_fwd_kernel<N, T, CPT, DT, FUSE>;
+  const size_t smem = sizeof(FwdSmem<T, N>);
+  auto kern = scan_fwd_kernel<N, T, FUSE, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
-  // prefer the largest shared-memory carveout, so that residency (and the occupancy
-  // query the segment and grid choices rely on) is limited by the CTAs' own needs
   cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-  // segments: only when (batch row, channel tile) pairs leave SMs idle
+  // segments: only when (batch row, channel tile) warps leave SMs idle
   p.P = 1;
   p.Ls = p.L;
   const int pmax = fwd_pmax<N>(p.B, p.L, p.D);
   if (pmax > 1) {
-    int per_sm = 0;
-    per_sm = resident_ctas(kern, GeoF<N, CPT, DT>::NT, smem);
+    const int per_sm = resident_ctas(kern, 32, smem);
     if (per_sm < 1) return SS_ERR_CUDA;
     const long long resident = (long long)per_sm * device_sm_count();
     int want = (int)(resident / ((long long)ndt * p.B));
@@ -484,28 +326,28 @@ int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, co
     const SegPlan sp = seg_plan(want, p.L, kTT);
     p.P = sp.P;
     p.Ls = sp.Ls;
+    const FwdWs wl = fwd_ws_layout(p.B, p.D, N, pmax);
     p.hsum = static_cast<float*>(ws);
-    p.dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + (((size_t)p.B * pmax * p.D * N * sizeof(float) + 255) & ~(size_t)255));
+    p.dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.off_dsum);
+    p.hin = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.off_hin);
   }
   if (p.P > 1) {
-    const size_t smem_s = sizeof(FwdSumSmem<T, N, DT>);
-    auto skern = scan_fwd_summary_kernel<N, T, CPT, DT, FUSE>;
-    if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s) != cudaSuccess)
+    auto skern = scan_fwd_kernel<N, T, FUSE, true>;
+    if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return SS_ERR_CUDA;
-  // prefer the largest shared-memory carveout, so that residency (and the occupancy
-  // query the segment and grid choices rely on) is limited by the CTAs' own needs
-  cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-    skern<<<dim3(ndt, p.B * (p.P - 1)), GeoF<N, CPT, DT>::NT, smem_s, stream>>>(p, tm[0], tm[1], tm[3]);
+    cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    skern<<<dim3(ndt, p.B * (p.P - 1)), 32, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
     if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
-    kern<<<dim3(ndt, p.B * p.P), GeoF<N, CPT, DT>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
+    if (seg_combine<false>(SegCombine{p.A, p.dsum, p.hsum, p.h0, p.hin, p.P, p.D, N}, p.B, stream) != cudaSuccess)
+      return SS_ERR_CUDA;
+    kern<<<dim3(ndt, p.B * p.P), 32, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
   } else {
-    const int cap = 1024 / ndt > 0 ? 1024 / ndt : 1;  // about 1024 CTAs; each loops over its batch rows
+    const int cap = 8192 / ndt > 0 ? 8192 / ndt : 1;  // at most ~8192 CTAs; each loops over its batch rows
     const int gy = p.B < cap ? p.B : cap;
-    kern<<<dim3(ndt, gy), GeoF<N, CPT, DT>::NT, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
+    kern<<<dim3(ndt, gy), 32, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
   }
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
-
 }  // namespace
 
 namespace ssh {
@@ -563,7 +405,7 @@ extern "C" int ss_scan_fwd(const void* x, const void* delta, const float* A, con
   const size_t need = fwd_ws_bytes(B, L, D, N);
   if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SS_ERR_WORKSPACE;
   if (workspace != nullptr && !ssh::aligned16(workspace)) return SS_ERR_ALIGN;
-  FwdParams p{A, Dv, h0, y, ckpt, h_last, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 1, L, nullptr, nullptr,
+  FwdParams p{A, Dv, h0, y, ckpt, h_last, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 1, L, nullptr, nullptr, nullptr,
               dt_bias, delta_softplus ? 1 : 0, (dt_bias != nullptr || delta_softplus) ? 1 : 0};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SS_F32) {

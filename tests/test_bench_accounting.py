@@ -29,3 +29,13 @@ def test_side_kernel_bytes():
     E = 4 * 2048 * 4096
     assert abs(a["conv1d_bwd"] - E * (4 + 2 + 4)) < 1e6          # read g fp32, x bf16; write dx fp32
     assert abs(a["rmsnorm_bwd"] - 8192 * 2048 * (2 + 2 + 4)) < 1e6  # read dy, x bf16; write dx fp32
+
+
+def test_checkpoint_overhead():
+    """At a checkpoint every 8 steps the 1.4B layer's scan writes (forward) and reads (backward) all
+    2048/8 = 256 checkpoints of B*D*N fp32 = 1 MiB each (268.4 MB); the count allows 2048/256 - 1 = 7 (7.3 MB)."""
+    import bench
+    wl = CONFIGS["mamba1p4b"]
+    got = bench.checkpoint_overhead_bytes(wl, 8)
+    assert got == 4 * 4096 * 16 * 4 * (256 - 7)
+    assert bench.checkpoint_overhead_bytes(CONFIGS["long"], 256) == 1 * 2048 * 16 * 4  # only the first
