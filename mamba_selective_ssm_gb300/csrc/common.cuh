@@ -293,21 +293,33 @@ constexpr unsigned kErrTmaTimeout = 1u;
 
 // Column sums of a [rows, ncols] fp32 partial array in a fixed order:
 // out(i) = sum_{g < rows} part[g * ncols + i], delivered to Store::put(i, v).
-// Block (32, 8): thread (x, y) adds rows g = y, y+8, ... in ascending order,
-// then the eight partial sums are added y = 0..7; deterministic run to run.
-template <class Store>
-__global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ part, long long ncols, int rows, Store st) {
-  __shared__ float red[8][33];
+// Block (32, RG): thread (x, y) adds rows g = y, y+RG, ... in ascending order
+// (loads issued four at a time, adds in that order), then the RG partial sums
+// are added y = 0..RG-1; deterministic run to run.  RG = 32 when the columns
+// alone give too few blocks to fill the GPU.
+template <class Store, int RG>
+__global__ void __launch_bounds__(32 * RG) colsum_kernel(const float* __restrict__ part, long long ncols, int rows, Store st) {
+  __shared__ float red[RG][33];
   const long long i = (long long)blockIdx.x * 32 + threadIdx.x;
   float acc = 0.f;
-  if (i < ncols)
-    for (int g = threadIdx.y; g < rows; g += 8) acc += part[(size_t)g * ncols + i];
+  if (i < ncols) {
+    int g = threadIdx.y;
+    for (; g + 3 * RG < rows; g += 4 * RG) {
+      const float v0 = part[(size_t)g * ncols + i], v1 = part[(size_t)(g + RG) * ncols + i];
+      const float v2 = part[(size_t)(g + 2 * RG) * ncols + i], v3 = part[(size_t)(g + 3 * RG) * ncols + i];
+      acc += v0;
+      acc += v1;
+      acc += v2;
+      acc += v3;
+    }
+    for (; g < rows; g += RG) acc += part[(size_t)g * ncols + i];
+  }
   red[threadIdx.y][threadIdx.x] = acc;
   __syncthreads();
   if (threadIdx.y == 0 && i < ncols) {
     float v = red[0][threadIdx.x];
 #pragma unroll
-    for (int y = 1; y < 8; ++y) v += red[y][threadIdx.x];
+    for (int y = 1; y < RG; ++y) v += red[y][threadIdx.x];
     st.put(i, v);
   }
 }
@@ -315,7 +327,10 @@ __global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ p
 template <class Store>
 inline cudaError_t colsum(const float* part, long long ncols, int rows, Store st, cudaStream_t s) {
   const long long blocks = (ncols + 31) / 32;
-  colsum_kernel<Store><<<(unsigned)blocks, dim3(32, 8), 0, s>>>(part, ncols, rows, st);
+  if (blocks < 4ll * device_sm_count() && rows >= 64)
+    colsum_kernel<Store, 32><<<(unsigned)blocks, dim3(32, 32), 0, s>>>(part, ncols, rows, st);
+  else
+    colsum_kernel<Store, 8><<<(unsigned)blocks, dim3(32, 8), 0, s>>>(part, ncols, rows, st);
   return cudaGetLastError();
 }
 

@@ -10,9 +10,11 @@
 // row parity.  Rows reach the CTA through a ring of `nst` shared-memory stages
 // filled by untiled bulk copies (cp.async.bulk, one mbarrier per stage), so
 // up to nst rows of dy and x per CTA are in flight without holding registers
-// (rms_bwd_tma_kernel); the register-prefetch form (rms_bwd_kernel, one row
-// ahead) serves the fixed-grid no-alloc entry point and rows too wide for two
-// stages.  Per-CTA dscale partials are added in fixed order by colsum_kernel.
+// (rms_bwd_tma_kernel, rows of 2049 .. 8192 columns); rows of 257 .. 2048
+// columns go one warp per row (rms_bwd_warp_kernel, no block barrier per row);
+// the register-prefetch form (rms_bwd_kernel, one row ahead) serves the
+// fixed-grid no-alloc entry point and rows too wide for two stages.  Per-CTA
+// dscale partials are added in fixed order by colsum_kernel.
 #include <mutex>
 
 #include "common.cuh"
@@ -164,6 +166,13 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_tma_kernel(const T* __
         atomicOr(&g_rms_err, kErrTmaTimeout);
         for (int k2 = k; k2 < k + nst && k2 < nk; ++k2) mbar_wait_bounded(&full[k2 % nst], (k2 / nst) & 1, 100000000ull);
       }
+      // the column sum still adds this CTA's partial row: make it zero
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int c = (v * blockDim.x + tid) * 8;
+        const float z8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (col_ok[v]) ActT<float>::st8(ws + (size_t)blockIdx.x * dim + c, z8);
+      }
       return;
     }
     float gy[VPT][8], xv[VPT][8];
@@ -209,6 +218,128 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_tma_kernel(const T* __
   for (int v = 0; v < VPT; ++v) {
     const int c = (v * blockDim.x + tid) * 8;
     if (col_ok[v]) ActT<float>::st8(ws + (size_t)blockIdx.x * dim + c, acc[v]);
+  }
+}
+
+// Rows of 257 .. 2048 columns: one warp per row, no block barrier.  Lane l owns
+// the 8-column groups l, l + 32, ... (VPW of them), keeps scale and its dscale
+// partial sums in registers, and reads the row twice from its warp's ring of
+// shared-memory stages (bulk copies, one mbarrier per stage): once for the dot
+// product, reduced with shuffles, and once for dx.  The CTA's warps add their
+// dscale partials in fixed order at the end; a warp that gave up on a wait
+// contributes zeros (its outputs are invalid and ss_device_status reports it).
+constexpr int kRmsWarps = 4;
+
+template <typename T, int VPW>
+__global__ void __launch_bounds__(32 * kRmsWarps) rms_bwd_warp_kernel(const T* __restrict__ dy, const T* __restrict__ x,
+                                                                      const float* __restrict__ scale,
+                                                                      const float* __restrict__ rms,
+                                                                      float* __restrict__ dx, float* __restrict__ ws,
+                                                                      int rows, int dim, int nst) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t row_bytes = (uint32_t)dim * sizeof(T);
+  T* buf = reinterpret_cast<T*>(sm) + (size_t)warp * nst * 2 * dim;  // this warp's [nst][dy | x][dim]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)kRmsWarps * nst * 2 * row_bytes) + warp * nst;
+  const long long nwarps = (long long)gridDim.x * kRmsWarps;
+  const long long gw = (long long)blockIdx.x * kRmsWarps + warp;
+  const int nk = gw < rows ? (int)((rows - gw + nwarps - 1) / nwarps) : 0;  // rows of this warp
+  auto issue = [&](int k) {  // lane 0; the stage's readers passed a warp sync
+    fence_proxy_async_smem();
+    const size_t r = (size_t)(gw + (long long)k * nwarps);
+    const int st = k % nst;
+    mbar_arrive_expect_tx(&full[st], 2 * row_bytes);
+    bulk_load(buf + (size_t)(2 * st) * dim, dy + r * dim, row_bytes, &full[st]);
+    bulk_load(buf + (size_t)(2 * st + 1) * dim, x + r * dim, row_bytes, &full[st]);
+  };
+  if (lane == 0) {
+    for (int st = 0; st < nst; ++st) mbar_init(&full[st], 1);
+    fence_barrier_init();
+    for (int k = 0; k < nst && k < nk; ++k) issue(k);
+  }
+  float sc[VPW][8], acc[VPW][8];
+#pragma unroll
+  for (int v = 0; v < VPW; ++v) {
+    const int c = (v * 32 + lane) * 8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sc[v][e] = c < dim ? scale[c + e] : 0.f;
+      acc[v][e] = 0.f;
+    }
+  }
+  __syncwarp();
+  const float inv_dim = 1.0f / (float)dim;
+  bool failed = false;
+  float rms_next = nk > 0 ? rms[gw] : 1.f;  // the row's rms, read one row ahead
+  for (int k = 0; k < nk; ++k) {
+    const long long r = gw + (long long)k * nwarps;
+    const int st = k % nst;
+    const float inv = 1.0f / rms_next;
+    if (k + 1 < nk) rms_next = rms[r + nwarps];
+    const bool ok = mbar_wait_bounded(&full[st], (k / nst) & 1, kWaitLimitNs);
+    if (__any_sync(0xffffffffu, !ok)) {
+      if (lane == 0) {
+        atomicOr(&g_rms_err, kErrTmaTimeout);
+        for (int k2 = k; k2 < k + nst && k2 < nk; ++k2) mbar_wait_bounded(&full[k2 % nst], (k2 / nst) & 1, 100000000ull);
+      }
+      failed = true;
+      break;
+    }
+    const T* g_s = buf + (size_t)(2 * st) * dim;
+    const T* x_s = buf + (size_t)(2 * st + 1) * dim;
+    float part = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPW; ++v) {
+      const int c = (v * 32 + lane) * 8;
+      if (c < dim) {
+        float gv[8], xv[8];
+        ActT<T>::ld8(g_s + c, gv);
+        ActT<T>::ld8(x_s + c, xv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part = fmaf(gv[e] * sc[v][e], xv[e], part);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    const float kk = part * inv * inv * inv_dim;
+#pragma unroll
+    for (int v = 0; v < VPW; ++v) {
+      const int c = (v * 32 + lane) * 8;
+      if (c < dim) {
+        float gv[8], xv[8], o[8];
+        ActT<T>::ld8(g_s + c, gv);
+        ActT<T>::ld8(x_s + c, xv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          o[e] = inv * (sc[v][e] * gv[e]) - inv * (xv[e] * kk);
+          acc[v][e] = fmaf(gv[e] * xv[e], inv, acc[v][e]);
+        }
+        ActT<float>::st8(dx + (size_t)r * dim + c, o);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && k + nst < nk) issue(k + nst);
+  }
+  if (failed) {
+#pragma unroll
+    for (int v = 0; v < VPW; ++v)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[v][e] = 0.f;
+  }
+  // the CTA's dscale partial row: the warps' sums added in warp order (the stages are free now)
+  __syncthreads();
+  float* red = reinterpret_cast<float*>(sm);  // [kRmsWarps][dim], within the stage buffers
+#pragma unroll
+  for (int v = 0; v < VPW; ++v) {
+    const int c = (v * 32 + lane) * 8;
+    if (c < dim) ActT<float>::st8(red + (size_t)warp * dim + c, acc[v]);
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < dim; c += 32 * kRmsWarps) {
+    float a = red[c];
+#pragma unroll
+    for (int w = 1; w < kRmsWarps; ++w) a += red[(size_t)w * dim + c];
+    ws[(size_t)blockIdx.x * dim + c] = a;
   }
 }
 
@@ -358,6 +489,39 @@ int rms_tma_launch(const void* dy, const void* x, const float* scale, const floa
   return run(rms_bwd_tma_kernel<T, 1>);
 }
 
+// The warp-per-row form: up to 4 stages per warp within ~100 KB per CTA, as many CTAs as fit (at most the
+// workspace's partial rows); the dscale partial rows are added by colsum_kernel.
+template <typename T>
+int rms_warp_launch(const void* dy, const void* x, const float* scale, const float* rms, float* dx, float* dscale,
+                    int rows, int dim, float* ws, const RmsPlan& pl, cudaStream_t s) {
+  const size_t pair = (size_t)2 * dim * sizeof(T);
+  int nst = (int)((100u * 1024u) / (kRmsWarps * pair));
+  if (nst > 4) nst = 4;
+  if (nst < 2) nst = 2;
+  size_t smem = (size_t)kRmsWarps * nst * pair + (size_t)kRmsWarps * nst * sizeof(uint64_t);
+  if (smem < (size_t)kRmsWarps * dim * sizeof(float)) smem = (size_t)kRmsWarps * dim * sizeof(float);  // the final sum
+  const T* g = static_cast<const T*>(dy);
+  const T* xx = static_cast<const T*>(x);
+  auto run = [&](auto kern) -> int {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
+    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    const int per_sm = resident_ctas(kern, 32 * kRmsWarps, smem);
+    if (per_sm < 1) return SS_ERR_CUDA;
+    long long grid = (long long)per_sm * device_sm_count();
+    const long long need = ((long long)rows + kRmsWarps - 1) / kRmsWarps;
+    if (grid > need) grid = need;
+    if (grid > pl.grid) grid = pl.grid;  // the workspace holds pl.grid partial rows
+    if (grid < 1) grid = 1;
+    kern<<<(int)grid, 32 * kRmsWarps, smem, s>>>(g, xx, scale, rms, dx, ws, rows, dim, nst);
+    if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+    return colsum(ws, dim, (int)grid, AddTo{dscale}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  };
+  const int vpw = (dim + 255) / 256;
+  if (vpw <= 2) return run(rms_bwd_warp_kernel<T, 2>);
+  if (vpw <= 4) return run(rms_bwd_warp_kernel<T, 4>);
+  return run(rms_bwd_warp_kernel<T, 8>);
+}
+
 template <typename T>
 int rms_launch(const void* dy, const void* x, const float* scale, const float* rms, float* dx, float* dscale, int rows,
                int dim, float* ws, const RmsPlan& pl, cudaStream_t s) {
@@ -393,6 +557,10 @@ extern "C" int rmsnorm_bwd(const void* dy, const void* x, const float* scale, co
   if (dim <= 256) {  // short rows: several rows per warp
     if (dtype == SS_F32) return rms_small_dispatch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
     return rms_small_dispatch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+  }
+  if (dim <= 2048) {  // one warp per row
+    if (dtype == SS_F32) return rms_warp_launch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+    return rms_warp_launch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
   }
   const int nst = rms_tma_stages(dim, dtype == SS_F32 ? 4 : 2);
   if (nst > 0 && pl.vpt == 1) {  // dim <= 8192 and two stages fit

@@ -7,7 +7,9 @@
 // 8 consecutive columns; the row's sum of squares is reduced with warp
 // shuffles and one shared-memory exchange whose buffer alternates with the
 // row parity; y is written in the input dtype (bf16 rounded to nearest even)
-// and rms_r in fp32.  Rows of at most 8192 columns arrive through a ring of
+// and rms_r in fp32.  Rows of 257 .. 2048 columns go one warp per row through
+// a per-warp ring of bulk-copied stages (rms_fwd_warp_kernel, no block barrier
+// per row); rows of at most 8192 columns arrive through a per-CTA ring of
 // shared-memory stages filled by untiled bulk copies (rms_fwd_tma_kernel);
 // wider rows use the register-prefetch form (one row ahead).
 #include "common.cuh"
@@ -163,6 +165,118 @@ __global__ void __launch_bounds__(kRmsFMaxThreads) rms_fwd_tma_kernel(const T* _
   }
 }
 
+// Rows of 257 .. 2048 columns: one warp per row, no block barrier.  Lane l
+// owns the 8-column groups l, l + 32, ... (VPW of them) and reads the row
+// twice from its warp's ring of shared-memory stages (bulk copies, one
+// mbarrier per stage): once for the sum of squares, reduced with shuffles, and
+// once for y.
+constexpr int kRmsFWarps = 4;
+
+template <typename T, int VPW>
+__global__ void __launch_bounds__(32 * kRmsFWarps) rms_fwd_warp_kernel(const T* __restrict__ x,
+                                                                       const float* __restrict__ scale, float eps,
+                                                                       T* __restrict__ y, float* __restrict__ rms, int rows,
+                                                                       int dim, int nst) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t row_bytes = (uint32_t)dim * sizeof(T);
+  T* buf = reinterpret_cast<T*>(sm) + (size_t)warp * nst * dim;  // this warp's [nst][dim]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)kRmsFWarps * nst * row_bytes) + warp * nst;
+  const long long nwarps = (long long)gridDim.x * kRmsFWarps;
+  const long long gw = (long long)blockIdx.x * kRmsFWarps + warp;
+  const int nk = gw < rows ? (int)((rows - gw + nwarps - 1) / nwarps) : 0;
+  auto issue = [&](int k) {  // lane 0; the stage's readers passed a warp sync
+    fence_proxy_async_smem();
+    const size_t r = (size_t)(gw + (long long)k * nwarps);
+    const int st = k % nst;
+    mbar_arrive_expect_tx(&full[st], row_bytes);
+    bulk_load(buf + (size_t)st * dim, x + r * dim, row_bytes, &full[st]);
+  };
+  if (lane == 0) {
+    for (int st = 0; st < nst; ++st) mbar_init(&full[st], 1);
+    fence_barrier_init();
+    for (int k = 0; k < nst && k < nk; ++k) issue(k);
+  }
+  float sc[VPW][8];
+#pragma unroll
+  for (int v = 0; v < VPW; ++v) {
+    const int c = (v * 32 + lane) * 8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sc[v][e] = c < dim ? scale[c + e] : 0.f;
+  }
+  __syncwarp();
+  const float inv_dim = 1.0f / (float)dim;
+  for (int k = 0; k < nk; ++k) {
+    const long long r = gw + (long long)k * nwarps;
+    const int st = k % nst;
+    const bool ok = mbar_wait_bounded(&full[st], (k / nst) & 1, kWaitLimitNs);
+    if (__any_sync(0xffffffffu, !ok)) {
+      if (lane == 0) {
+        atomicOr(&g_rmsf_err, kErrTmaTimeout);
+        for (int k2 = k; k2 < k + nst && k2 < nk; ++k2) mbar_wait_bounded(&full[k2 % nst], (k2 / nst) & 1, 100000000ull);
+      }
+      return;
+    }
+    const T* x_s = buf + (size_t)st * dim;
+    float part = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPW; ++v) {
+      const int c = (v * 32 + lane) * 8;
+      if (c < dim) {
+        float xv[8];
+        ActT<T>::ld8(x_s + c, xv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part = fmaf(xv[e], xv[e], part);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    const float rr = sqrtf(fmaf(part, inv_dim, eps));
+    const float inv = 1.0f / rr;
+    if (lane == 0 && rms != nullptr) rms[r] = rr;
+#pragma unroll
+    for (int v = 0; v < VPW; ++v) {
+      const int c = (v * 32 + lane) * 8;
+      if (c < dim) {
+        float xv[8], o[8];
+        ActT<T>::ld8(x_s + c, xv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = (xv[e] * sc[v][e]) * inv;
+        ActT<T>::st8(y + (size_t)r * dim + c, o);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && k + nst < nk) issue(k + nst);
+  }
+}
+
+template <typename T>
+int rms_fwd_warp_launch(const void* x, const float* scale, float eps, void* y, float* rms, int rows, int dim,
+                        cudaStream_t s) {
+  const size_t rb = (size_t)dim * sizeof(T);
+  int nst = (int)((64u * 1024u) / (kRmsFWarps * rb));
+  if (nst > 4) nst = 4;
+  if (nst < 2) nst = 2;
+  const size_t smem = (size_t)kRmsFWarps * nst * rb + (size_t)kRmsFWarps * nst * sizeof(uint64_t);
+  auto run = [&](auto kern) -> int {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
+    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    const int per_sm = resident_ctas(kern, 32 * kRmsFWarps, smem);
+    if (per_sm < 1) return SS_ERR_CUDA;
+    long long grid = (long long)per_sm * device_sm_count();
+    const long long need = ((long long)rows + kRmsFWarps - 1) / kRmsFWarps;
+    if (grid > need) grid = need;
+    if (grid < 1) grid = 1;
+    kern<<<(int)grid, 32 * kRmsFWarps, smem, s>>>(static_cast<const T*>(x), scale, eps, static_cast<T*>(y), rms, rows, dim,
+                                                   nst);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  };
+  const int vpw = (dim + 255) / 256;
+  if (vpw <= 2) return run(rms_fwd_warp_kernel<T, 2>);
+  if (vpw <= 4) return run(rms_fwd_warp_kernel<T, 4>);
+  return run(rms_fwd_warp_kernel<T, 8>);
+}
+
 // Rows of at most 256 columns: G lanes per row (one 8-column group each), 32/G
 // rows per warp, the sum of squares reduced by shuffles inside each G-lane
 // segment, no block barrier per row.
@@ -239,6 +353,7 @@ int rms_fwd_launch(const void* x, const float* scale, float eps, void* y, float*
     if (groups <= 16) return rms_fwd_small_launch<T, 16>(x, scale, eps, y, rms, rows, dim, s);
     return rms_fwd_small_launch<T, 32>(x, scale, eps, y, rms, rows, dim, s);
   }
+  if (groups <= 256) return rms_fwd_warp_launch<T>(x, scale, eps, y, rms, rows, dim, s);  // one warp per row
   if (groups <= 1024) {  // one 8-column group per thread: the bulk-copy ring, up to 16 rows or ~100 KB per CTA
     int nst = (int)((32u * 1024u) / ((size_t)dim * sizeof(T)));
     if (nst > 16) nst = 16;

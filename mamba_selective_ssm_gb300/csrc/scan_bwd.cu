@@ -783,7 +783,8 @@ __global__ void __launch_bounds__(256) ss_bwd_reduce_kernel(const float* __restr
   if ((int)blockIdx.x < nblk_bc) {
     for (long long i = blockIdx.x * 256ll + threadIdx.x; i < nBC; i += (long long)nblk_bc * 256) {
       float acc = 0.f;
-      for (int t = 0; t < ndt; ++t) acc += ws_dBC[(size_t)t * nBC + i];
+#pragma unroll 8
+      for (int t = 0; t < ndt; ++t) acc += ws_dBC[(size_t)t * nBC + i];  // loads ahead, adds in tile order
       const long long row = i / (2 * N);
       const int c = (int)(i % (2 * N));
       if (c < N) dB[row * N + c] = acc;
@@ -795,8 +796,10 @@ __global__ void __launch_bounds__(256) ss_bwd_reduce_kernel(const float* __restr
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const long long i = (long long)(blockIdx.x - nblk_bc) * 32 + tx;
   float acc = 0.f;
-  if (i < nAD)
+  if (i < nAD) {
+#pragma unroll 4
     for (int g = ty; g < rows; g += 8) acc += ws_dAD[(size_t)g * nAD + i];
+  }
   red[ty][tx] = acc;
   __syncthreads();
   if (ty == 0 && i < nAD) {

@@ -1,13 +1,15 @@
 """rmsnorm_bwd_noalloc: the RMSNorm backward for callers that cannot allocate
 device memory (its scratch is a fixed array inside the library).  Called
 through the C ABI, twice in a row, and compared with rmsnorm_bwd, which takes
-a caller-allocated workspace.  This file is collected last on purpose."""
+a caller-allocated workspace, and with the float64 oracle.  This file is
+collected last on purpose."""
 
 import ctypes
 
 import numpy as np
 import pytest
 
+from oracle import rmsnorm_bwd_ref
 from tests._util import TOL, assert_close
 from tests.gpu_util import dev, host, ss_module
 from workloads import CONFIGS, make_rmsnorm_inputs
@@ -35,6 +37,7 @@ def test_noalloc_matches_allocating_entry_point(rows, dim, dtype):
     ws = torch.empty(lib.rmsnorm_bwd_workspace_size(rows, dim), device="cuda", dtype=torch.uint8)
     assert lib.rmsnorm_bwd(p(dy), p(x), p(scale), p(rms), p(ref_dx), p(ref_ds), rows, dim, sdt, p(ws), ws.numel(),
                            stream) == 0
+    odx, ods = rmsnorm_bwd_ref(r["dy"], r["x"], r["scale"], r["rms"])
     for _ in range(2):  # the shared scratch keeps the previous call's partials
         dx = torch.full((rows, dim), float("nan"), device="cuda")
         ds = torch.zeros(dim, device="cuda")
@@ -42,6 +45,9 @@ def test_noalloc_matches_allocating_entry_point(rows, dim, dtype):
         torch.cuda.synchronize()
         assert_close(host(dx), host(ref_dx), TOL["f32"], "dx")
         assert_close(host(ds), host(ref_ds), TOL["f32"], "dscale")
+        # and against the float64 oracle itself, at the parity bar of the other RMSNorm tests
+        assert_close(host(dx), odx, TOL["f32"], "dx vs oracle")
+        assert_close(host(ds), ods, TOL["f32"], "dscale vs oracle")
 
 
 def test_noalloc_rejects_dim_beyond_its_scratch():
