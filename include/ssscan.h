@@ -151,6 +151,65 @@ int ss_scan_bwd(const void* x, const void* delta, const float* A, const void* Bm
                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Sequence sharding.  The recurrence of ss_scan_fwd over steps t0 .. t1-1 of a
+ * channel is an affine map of the state entering the piece,
+ *     h -> exp(A * sum_t delta_t) * h + h_end,
+ * where h_end is the state the piece reaches from a zero start: the product
+ * of the a_t over the piece is the exponential of A times the piece's sum of
+ * delta.  The adjoint of ss_scan_bwd is the same map run the other way,
+ *     g -> exp(A * sum_t delta_t) * g + g_start,
+ * from the carry arriving at the piece's end to the adjoint it sends out of its
+ * first step (g_start: that adjoint when nothing arrives, i.e. a_0 * G_0 of the
+ * piece with dh_last = 0).  Composing these maps over the pieces in order
+ * (ss_scan_carries) gives every piece the state (forward) or carry (backward)
+ * it starts from; ss_scan_fwd with h0 = that state and ss_scan_bwd with
+ * dh_last = that carry then give each piece exactly its part of the scan over
+ * the whole sequence (up to rounding order), so that a sequence cut along
+ * time over P ranks needs one exchange of [B, D, N] + [B, D] per pass.
+ *
+ * ss_scan_fwd_summary — one piece's forward summary:
+ *   x, delta : [B, L, D];  Bm : [B, L, N]  (dtype; the piece's steps only)
+ *   A        : [D, N] fp32
+ *   h_end    : [B, D, N] fp32 output, the state after the piece's last step from h = 0
+ *   delta_sum: [B, D]    fp32 output, sum over the piece of delta (after the
+ *              fused discretisation dt_bias / delta_softplus, as in ss_scan_fwd)
+ * Sizes, dtypes and alignment as ss_scan_fwd; no workspace.
+ */
+int ss_scan_fwd_summary(const void* x, const void* delta, const float* A, const void* Bm,
+                        float* h_end, float* delta_sum, int B, int L, int D, int N, int dtype,
+                        const float* dt_bias, int delta_softplus, void* stream);
+
+/*
+ * ss_scan_bwd_summary — one piece's backward summary:
+ *   delta, z, dy : [B, L, D];  Cm : [B, L, N]  (dtype; the piece's steps only)
+ *   A        : [D, N] fp32
+ *   g_start  : [B, D, N] fp32 output, what ss_scan_bwd would give as dh0 for
+ *              the piece with dh_last NULL
+ *   delta_sum: [B, D] fp32 output, as in ss_scan_fwd_summary
+ * Sizes, dtypes and alignment as ss_scan_bwd; no workspace.
+ */
+int ss_scan_bwd_summary(const void* delta, const float* A, const void* Cm, const void* z, const void* dy,
+                        float* g_start, float* delta_sum, int B, int L, int D, int N, int dtype,
+                        const float* dt_bias, int delta_softplus, void* stream);
+
+/*
+ * ss_scan_carries — composes the P pieces' maps (piece-major arrays, as an
+ * all-gather over ranks delivers them):
+ *   delta_sum : [P, B, D]    fp32, summ : [P, B, D, N] fp32 (h_end or g_start)
+ *   init      : [B, D, N]    fp32 carry entering the whole scan (h0 forward,
+ *               dh_last backward), or NULL for zeros
+ *   carry     : [P, B, D, N] fp32 output
+ *   reverse 0 (forward):  carry[0] = init,   carry[p+1] = exp(A*delta_sum[p]) * carry[p] + summ[p]
+ *   reverse 1 (backward): carry[P-1] = init, carry[p-1] = exp(A*delta_sum[p]) * carry[p] + summ[p]
+ * so carry[p] is the state entering piece p (forward) or the carry arriving at
+ * its end (backward); summ[P-1] (forward) and summ[0] (backward) are not read.
+ * The maps are composed by an associative scan in the kernel.
+ * 1 <= P <= 64 (else SS_ERR_UNSUPPORTED); B < 65536; pointers 4-byte aligned.
+ */
+int ss_scan_carries(const float* A, const float* delta_sum, const float* summ, const float* init, float* carry,
+                    int P, int B, int D, int N, int reverse, void* stream);
+
+/*
  * Workspace bytes conv1d_causal_bwd needs (0 on invalid sizes).
  */
 size_t conv1d_causal_bwd_workspace_size(int B, int L, int D, int d_conv);

@@ -34,6 +34,9 @@ SIGNATURES = {
     "ss_scan_fwd": (_i, [_vp] * 11 + [_i] * 6 + [_vp, _i, _vp, _sz, _vp]),
     "ss_scan_bwd_workspace_size": (_sz, [_i] * 6),
     "ss_scan_bwd": (_i, [_vp] * 18 + [_i] * 6 + [_vp, _i, _vp, _vp, _sz, _vp]),
+    "ss_scan_fwd_summary": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _i, _vp]),
+    "ss_scan_bwd_summary": (_i, [_vp] * 7 + [_i] * 5 + [_vp, _i, _vp]),
+    "ss_scan_carries": (_i, [_vp] * 5 + [_i] * 5 + [_vp]),
     "conv1d_causal_bwd_workspace_size": (_sz, [_i] * 4),
     "conv1d_causal_bwd": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _sz, _vp]),
     "conv1d_causal_silu_bwd": (_i, [_vp] * 7 + [_i] * 5 + [_vp, _sz, _vp]),

@@ -100,6 +100,7 @@ struct BwdParams {
   float* gsum;    // [B][P][D][N] adjoint a_tb G_tb at each segment's start from a zero carry at its end
   float* dsum;    // [B][P][D]    sum of delta over each segment
   float* gin;     // [B][P][D][N] carry a G arriving at the end of each segment (combine kernel output)
+  int sum_stride, sum_first;  // summary grid: rows per batch row and first segment (P and 1 inside ss_scan_bwd)
   const float* dt_bias;  // fused discretisation: delta = f(raw + dt_bias), f = softplus if dsp
   int dsp;
   int fuse;              // dt_bias != NULL or dsp
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
   const int dg = d0 + dl;
   const bool dvalid = dg < p.D;
   const int n0 = ng * 4;
-  const int b = (int)blockIdx.y / (p.P - 1), sgm = 1 + (int)blockIdx.y % (p.P - 1);
+  const int b = (int)blockIdx.y / (p.P - 1), sgm = p.sum_first + (int)blockIdx.y % (p.P - 1);
   const int tb = sgm * p.Ls, te = min(p.L, tb + p.Ls);
   const int gtb = tb / kTT, gte = (te + kTT - 1) / kTT;
   const int nitems = gte - gtb;
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
   if (dvalid) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const size_t row = ((size_t)b * p.P + sgm) * p.D + dg + j;
+      const size_t row = ((size_t)b * p.sum_stride + sgm) * p.D + dg + j;
       *reinterpret_cast<float4*>(p.gsum + row * N + n0) = make_float4(ga[j][0].x, ga[j][0].y, ga[j][1].x, ga[j][1].y);
       if (ng == 0) p.dsum[row] = dsum[j];
     }
@@ -912,6 +913,7 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
     const SegPlan sp = seg_plan(want, p.L, bwd_seg_unit(p.chunk));
     p.P = sp.P;
     p.Ls = sp.Ls;
+    p.sum_stride = sp.P;
   }
   int rows = pl.gy;
   if (p.P > 1) {
@@ -925,7 +927,7 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
   cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     skern<<<dim3(pl.ndt, p.B * (p.P - 1)), Geo<N, DT>::NT, smem_s, stream>>>(p, tm[0], tm[2], tm[3], tm[5]);
     if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
-    if (seg_combine<true>(SegCombine{p.A, p.dsum, p.gsum, p.dh_last, p.gin, p.P, p.D, N}, p.B, stream) != cudaSuccess)
+    if (seg_combine<true>(SegCombine{p.A, p.dsum, p.gsum, p.dh_last, p.gin, p.P, p.D, N, p.P, 1}, p.B, stream) != cudaSuccess)
       return SS_ERR_CUDA;
   }
   kern<<<dim3(pl.ndt, rows), Geo<N, DT>::NT, smem_launch, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4], tm[5]);
@@ -957,6 +959,42 @@ int validate_bwd(int B, int L, int D, int N, int chunk, int dtype) {
   if (((long long)L * N * (dtype == SS_F32 ? 4 : 2)) % 16 != 0) return SS_ERR_ALIGN;
   if ((long long)L * N >= (1ll << 31) || (long long)L * D >= (1ll << 40)) return SS_ERR_DIM;
   return SS_OK;
+}
+
+// One whole sequence summarised: the backward summary pass over the single segment [0, L) per batch row.
+template <int N, typename T, bool FUSE>
+int launch_bwd_summary(BwdParams p, const void* delta, const void* Cm, const void* z, const void* dy, cudaStream_t stream) {
+  constexpr int e = ActT<T>::kBytes;
+  constexpr int SDT = bwd_dt<N>();
+  const uint64_t adims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
+  const uint64_t astr[2] = {(uint64_t)p.D * e, (uint64_t)p.L * p.D * e};
+  const uint32_t sbox[3] = {SDT, kTT, 1};
+  const uint64_t bdims[2] = {(uint64_t)p.L * N, (uint64_t)p.B};
+  const uint64_t bstr[1] = {(uint64_t)p.L * N * e};
+  const uint32_t bbox[2] = {kTT * N, 1};
+  CUtensorMap tm[4];
+  if (!ssh::encode_tiled(&tm[0], ActT<T>::kTma, 3, delta, adims, astr, sbox) ||
+      !ssh::encode_tiled(&tm[1], ActT<T>::kTma, 3, z, adims, astr, sbox) ||
+      !ssh::encode_tiled(&tm[2], ActT<T>::kTma, 3, dy, adims, astr, sbox) ||
+      !ssh::encode_tiled(&tm[3], ActT<T>::kTma, 2, Cm, bdims, bstr, bbox))
+    return SS_ERR_CUDA;
+  const size_t smem_s = sizeof(BwdSumSmem<T, N, kSumStages, SDT>);
+  auto skern = scan_bwd_summary_kernel<N, T, kSumStages, SDT, FUSE>;
+  if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s) != cudaSuccess)
+    return SS_ERR_CUDA;
+  cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  p.P = 2;  // one summarised segment per batch row, starting at step 0
+  p.Ls = p.L;
+  p.sum_stride = 1;
+  p.sum_first = 0;
+  skern<<<dim3((p.D + SDT - 1) / SDT, p.B), Geo<N, SDT>::NT, smem_s, stream>>>(p, tm[0], tm[1], tm[2], tm[3]);
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+template <int N, typename T>
+int bwd_summary_fuse(const BwdParams& p, const void* delta, const void* Cm, const void* z, const void* dy, cudaStream_t s) {
+  return p.fuse ? launch_bwd_summary<N, T, true>(p, delta, Cm, z, dy, s)
+                : launch_bwd_summary<N, T, false>(p, delta, Cm, z, dy, s);
 }
 
 }  // namespace
@@ -992,7 +1030,7 @@ extern "C" int ss_scan_bwd(const void* x, const void* delta, const float* A, con
   if (workspace == nullptr || ws_bytes < pl.total) return SS_ERR_WORKSPACE;
   if (!ssh::aligned16(workspace)) return SS_ERR_ALIGN;
   BwdParams p{A, Dv, ckpt, dh_last, dx, ddelta, dz, dh0, nullptr, nullptr, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 0,
-              1, L, nullptr, nullptr, nullptr, dt_bias, delta_softplus ? 1 : 0,
+              1, L, nullptr, nullptr, nullptr, 1, 1, dt_bias, delta_softplus ? 1 : 0,
               (dt_bias != nullptr || delta_softplus) ? 1 : 0, d_dt_bias};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool wide = bwd_channels(N, chunk) == 64;
@@ -1010,4 +1048,27 @@ extern "C" int ss_scan_bwd(const void* x, const void* delta, const float* A, con
                 : launch_bwd<8, __nv_bfloat16>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
   return wide ? launch_bwd<16, __nv_bfloat16, Stages<__nv_bfloat16>::value, 64>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s)
               : launch_bwd<16, __nv_bfloat16>(p, x, delta, Bm, Cm, z, dy, dA, dB, dC, dD, workspace, s);
+}
+
+extern "C" int ss_scan_bwd_summary(const void* delta, const float* A, const void* Cm, const void* z, const void* dy,
+                                   float* g_start, float* delta_sum, int B, int L, int D, int N, int dtype,
+                                   const float* dt_bias, int delta_softplus, void* stream) {
+  if (!delta || !A || !Cm || !z || !dy || !g_start || !delta_sum) return SS_ERR_NULL;
+  const int v = validate_bwd(B, L, D, N, kTT, dtype);
+  if (v != SS_OK) return v;
+  const void* ptrs[] = {delta, A, Cm, z, dy, g_start, delta_sum};
+  for (const void* q : ptrs)
+    if (!ssh::aligned16(q)) return SS_ERR_ALIGN;
+  BwdParams p{A, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, L, D, kTT, 0, 0,
+              2, L, g_start, delta_sum, nullptr, 1, 0, dt_bias, delta_softplus ? 1 : 0,
+              (dt_bias != nullptr || delta_softplus) ? 1 : 0, nullptr};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == SS_F32) {
+    if (N == 4) return bwd_summary_fuse<4, float>(p, delta, Cm, z, dy, s);
+    if (N == 8) return bwd_summary_fuse<8, float>(p, delta, Cm, z, dy, s);
+    return bwd_summary_fuse<16, float>(p, delta, Cm, z, dy, s);
+  }
+  if (N == 4) return bwd_summary_fuse<4, __nv_bfloat16>(p, delta, Cm, z, dy, s);
+  if (N == 8) return bwd_summary_fuse<8, __nv_bfloat16>(p, delta, Cm, z, dy, s);
+  return bwd_summary_fuse<16, __nv_bfloat16>(p, delta, Cm, z, dy, s);
 }

@@ -119,6 +119,8 @@ struct SegCombine {
   const float* init;  // [B][D][N]    carry entering the scan (h0 or dh_last), or NULL
   float* out;         // [B][P][D][N]
   int P, D, N;
+  int sb, sv;         // row of (batch b, segment v) in dsum / summ / out: b * sb + v * sv
+                      // (sb = P, sv = 1 for the layout above; sb = 1, sv = B for segment-major [P][B])
 };
 
 template <bool REV>
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(256) seg_combine_kernel(const SegCombine c) {
   for (int v = ty; v < kSegMax; v += 8) {
     float a = 1.f, bv = 0.f;  // identity map where the scan has no segment
     if (ok && v < P - 1) {
-      const size_t row = (size_t)b * P + (REV ? P - 1 - v : v);
+      const size_t row = (size_t)b * c.sb + (size_t)(REV ? P - 1 - v : v) * c.sv;
       a = ex2(c.A[col] * kLog2e * c.dsum[row * c.D + col / c.N]);
       bv = c.summ[row * DN + col];
     }
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(256) seg_combine_kernel(const SegCombine c) {
   }
   __syncthreads();
   for (int v = ty; v < P; v += 8)
-    if (ok) c.out[((size_t)b * P + (REV ? P - 1 - v : v)) * DN + col] = al[v][tx];
+    if (ok) c.out[((size_t)b * c.sb + (size_t)(REV ? P - 1 - v : v) * c.sv) * DN + col] = al[v][tx];
 }
 
 template <bool REV>

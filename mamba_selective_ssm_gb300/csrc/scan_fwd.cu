@@ -45,6 +45,7 @@ struct FwdParams {
   float* hsum;   // [B][P][D][N] state at the end of each segment from a zero start
   float* dsum;   // [B][P][D]    sum of delta over each segment
   float* hin;    // [B][P][D][N] state entering each segment (combine kernel output)
+  int sum_stride;  // summary pass: rows of hsum / dsum per batch row (P inside ss_scan_fwd, 1 for one whole sequence)
   const float* dt_bias;  // fused discretisation: delta = f(raw + dt_bias), f = softplus if dsp
   int dsp;
   int fuse;              // dt_bias != NULL or dsp
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(32) scan_fwd_kernel(const FwdParams p, const _
       *reinterpret_cast<float4*>(p.h_last + ((size_t)b * p.D + dg) * N + n0) = make_float4(h0.x, h0.y, h1.x, h1.y);
   }
   if (SUM && dvalid) {
-    const size_t row = ((size_t)b_first * p.P + sgm) * p.D + dg;
+    const size_t row = ((size_t)b_first * p.sum_stride + sgm) * p.D + dg;
     *reinterpret_cast<float4*>(p.hsum + row * N + n0) = make_float4(h0.x, h0.y, h1.x, h1.y);
     if (ng == 0) p.dsum[row] = dsum;
   }
@@ -326,6 +327,7 @@ int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, co
     const SegPlan sp = seg_plan(want, p.L, kTT);
     p.P = sp.P;
     p.Ls = sp.Ls;
+    p.sum_stride = sp.P;
     const FwdWs wl = fwd_ws_layout(p.B, p.D, N, pmax);
     p.hsum = static_cast<float*>(ws);
     p.dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.off_dsum);
@@ -338,7 +340,7 @@ int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, co
     cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     skern<<<dim3(ndt, p.B * (p.P - 1)), 32, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
     if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
-    if (seg_combine<false>(SegCombine{p.A, p.dsum, p.hsum, p.h0, p.hin, p.P, p.D, N}, p.B, stream) != cudaSuccess)
+    if (seg_combine<false>(SegCombine{p.A, p.dsum, p.hsum, p.h0, p.hin, p.P, p.D, N, p.P, 1}, p.B, stream) != cudaSuccess)
       return SS_ERR_CUDA;
     kern<<<dim3(ndt, p.B * p.P), 32, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
   } else {
@@ -348,6 +350,38 @@ int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, co
   }
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
+// One whole sequence summarised: the summary pass over a single segment [0, L) per batch row.
+template <int N, typename T, bool FUSE>
+int launch_fwd_summary(FwdParams p, const void* x, const void* delta, const void* Bm, cudaStream_t stream) {
+  constexpr int e = ActT<T>::kBytes;
+  constexpr int DT = GeoW<N>::DT;
+  CUtensorMap tm[3];
+  const uint64_t adims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
+  const uint64_t astr[2] = {(uint64_t)p.D * e, (uint64_t)p.L * p.D * e};
+  const uint32_t abox[3] = {DT, kTT, 1};
+  const uint64_t bdims[2] = {(uint64_t)p.L * N, (uint64_t)p.B};
+  const uint64_t bstr[1] = {(uint64_t)p.L * N * e};
+  const uint32_t bbox[2] = {kTT * N, 1};
+  if (!ssh::encode_tiled(&tm[0], ActT<T>::kTma, 3, delta, adims, astr, abox) ||
+      !ssh::encode_tiled(&tm[1], ActT<T>::kTma, 3, x, adims, astr, abox) ||
+      !ssh::encode_tiled(&tm[2], ActT<T>::kTma, 2, Bm, bdims, bstr, bbox))
+    return SS_ERR_CUDA;
+  const size_t smem = sizeof(FwdSmem<T, N>);
+  auto skern = scan_fwd_kernel<N, T, FUSE, true>;
+  if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
+  cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  p.P = 2;  // one summarised segment per batch row
+  p.Ls = p.L;
+  p.sum_stride = 1;
+  skern<<<dim3((p.D + DT - 1) / DT, p.B), 32, smem, stream>>>(p, tm[0], tm[1], tm[1], tm[2], tm[2]);
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+template <int N, typename T>
+int fwd_summary_fuse(const FwdParams& p, const void* x, const void* delta, const void* Bm, cudaStream_t s) {
+  return p.fuse ? launch_fwd_summary<N, T, true>(p, x, delta, Bm, s) : launch_fwd_summary<N, T, false>(p, x, delta, Bm, s);
+}
+
 }  // namespace
 
 namespace ssh {
@@ -405,7 +439,7 @@ extern "C" int ss_scan_fwd(const void* x, const void* delta, const float* A, con
   const size_t need = fwd_ws_bytes(B, L, D, N);
   if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SS_ERR_WORKSPACE;
   if (workspace != nullptr && !ssh::aligned16(workspace)) return SS_ERR_ALIGN;
-  FwdParams p{A, Dv, h0, y, ckpt, h_last, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 1, L, nullptr, nullptr, nullptr,
+  FwdParams p{A, Dv, h0, y, ckpt, h_last, B, L, D, chunk, ss_scan_num_chunks(L, chunk), 1, L, nullptr, nullptr, nullptr, 1,
               dt_bias, delta_softplus ? 1 : 0, (dt_bias != nullptr || delta_softplus) ? 1 : 0};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SS_F32) {
@@ -416,4 +450,38 @@ extern "C" int ss_scan_fwd(const void* x, const void* delta, const float* A, con
   if (N == 4) return fwd_fuse<4, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
   if (N == 8) return fwd_fuse<8, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
   return fwd_fuse<16, __nv_bfloat16>(p, x, delta, Bm, Cm, z, workspace, s);
+}
+
+extern "C" int ss_scan_fwd_summary(const void* x, const void* delta, const float* A, const void* Bm, float* h_end,
+                                   float* delta_sum, int B, int L, int D, int N, int dtype, const float* dt_bias,
+                                   int delta_softplus, void* stream) {
+  if (!x || !delta || !A || !Bm || !h_end || !delta_sum) return SS_ERR_NULL;
+  const int v = validate_fwd(B, L, D, N, kTT, dtype);
+  if (v != SS_OK) return v;
+  const void* ptrs[] = {x, delta, A, Bm, h_end, delta_sum};
+  for (const void* q : ptrs)
+    if (!ssh::aligned16(q)) return SS_ERR_ALIGN;
+  FwdParams p{A, nullptr, nullptr, nullptr, nullptr, nullptr, B, L, D, kTT, 0, 2, L, h_end, delta_sum, nullptr, 1,
+              dt_bias, delta_softplus ? 1 : 0, (dt_bias != nullptr || delta_softplus) ? 1 : 0};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == SS_F32) {
+    if (N == 4) return fwd_summary_fuse<4, float>(p, x, delta, Bm, s);
+    if (N == 8) return fwd_summary_fuse<8, float>(p, x, delta, Bm, s);
+    return fwd_summary_fuse<16, float>(p, x, delta, Bm, s);
+  }
+  if (N == 4) return fwd_summary_fuse<4, __nv_bfloat16>(p, x, delta, Bm, s);
+  if (N == 8) return fwd_summary_fuse<8, __nv_bfloat16>(p, x, delta, Bm, s);
+  return fwd_summary_fuse<16, __nv_bfloat16>(p, x, delta, Bm, s);
+}
+
+extern "C" int ss_scan_carries(const float* A, const float* delta_sum, const float* summ, const float* init, float* carry,
+                               int P, int B, int D, int N, int reverse, void* stream) {
+  if (!A || !delta_sum || !summ || !carry) return SS_ERR_NULL;
+  if (B <= 0 || P <= 0 || D <= 0 || N <= 0) return SS_ERR_DIM;
+  if (P > kSegMax) return SS_ERR_UNSUPPORTED;
+  if ((long long)D * N >= (1ll << 31) || B >= 65536) return SS_ERR_DIM;
+  const SegCombine c{A, delta_sum, summ, init, carry, P, D, N, 1, B};  // segment-major [P][B]
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = reverse ? seg_combine<true>(c, B, s) : seg_combine<false>(c, B, s);
+  return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }

@@ -13,6 +13,10 @@ Names and argument order follow include/ssscan.h:
 * ``conv1d_causal_silu_bwd(dact, x, w, bias=None, dw=None, db=None)`` -> ``(dx, dw, db)``
 * ``rmsnorm_fwd(x, scale, eps)`` -> ``(y, rms)``
 * ``ss_scan_step(x, delta, A, Bm, Cm, Dv, z, h)`` -> ``y`` (h updated in place)
+* ``ss_scan_fwd_summary(x, delta, A, Bm)`` -> ``(h_end, delta_sum)``;
+  ``ss_scan_bwd_summary(delta, A, Cm, z, dy)`` -> ``(g_start, delta_sum)``;
+  ``ss_scan_carries(A, delta_sum, summ, init=None, reverse=False)`` -> ``carry``
+  (the pieces of a sequence-sharded scan; ``sharded.py`` runs them over ranks)
 * ``conv1d_causal_step(x, conv_state, w, bias=None, silu=False)`` -> ``out`` (state updated in place)
 
 Activations are ``torch.float32`` or ``torch.bfloat16`` CUDA tensors, contiguous;
@@ -154,6 +158,69 @@ def ss_scan_bwd(x, delta, A, Bm, Cm, Dv, z, ckpt, dy, dh_last=None, chunk: int =
                          workspace.numel() * workspace.element_size(), _stream())
     check(rc, "ss_scan_bwd")
     return out
+
+
+def ss_scan_fwd_summary(x, delta, A, Bm, dt_bias=None, delta_softplus: bool = False):
+    """Forward summary of one piece of a sequence -> ``(h_end [B,D,N], delta_sum [B,D])``:
+    the state the piece reaches from a zero start and its sum of (discretised) delta."""
+    lib = load()
+    B, L, D = x.shape
+    N = A.shape[1]
+    dev, dt = x.device, x.dtype
+    _act_dtype(x)
+    _req(x, "x", (B, L, D), dt, dev)
+    _req(delta, "delta", (B, L, D), dt, dev)
+    _req(Bm, "Bm", (B, L, N), dt, dev)
+    _req(A, "A", (D, N), torch.float32, dev)
+    if dt_bias is not None:
+        _req(dt_bias, "dt_bias", (D,), torch.float32, dev)
+    h_end = torch.empty((B, D, N), device=dev, dtype=torch.float32)
+    dsum = torch.empty((B, D), device=dev, dtype=torch.float32)
+    rc = lib.ss_scan_fwd_summary(_p(x), _p(delta), _p(A), _p(Bm), _p(h_end), _p(dsum), B, L, D, N, _DT[dt],
+                                 _p(dt_bias), int(bool(delta_softplus)), _stream())
+    check(rc, "ss_scan_fwd_summary")
+    return h_end, dsum
+
+
+def ss_scan_bwd_summary(delta, A, Cm, z, dy, dt_bias=None, delta_softplus: bool = False):
+    """Backward summary of one piece -> ``(g_start [B,D,N], delta_sum [B,D])``: the adjoint the
+    piece sends out of its first step when no carry arrives at its end, and its sum of delta."""
+    lib = load()
+    B, L, D = delta.shape
+    N = A.shape[1]
+    dev, dt = delta.device, delta.dtype
+    _act_dtype(delta)
+    for name, t in (("delta", delta), ("z", z), ("dy", dy)):
+        _req(t, name, (B, L, D), dt, dev)
+    _req(Cm, "Cm", (B, L, N), dt, dev)
+    _req(A, "A", (D, N), torch.float32, dev)
+    if dt_bias is not None:
+        _req(dt_bias, "dt_bias", (D,), torch.float32, dev)
+    g_start = torch.empty((B, D, N), device=dev, dtype=torch.float32)
+    dsum = torch.empty((B, D), device=dev, dtype=torch.float32)
+    rc = lib.ss_scan_bwd_summary(_p(delta), _p(A), _p(Cm), _p(z), _p(dy), _p(g_start), _p(dsum), B, L, D, N, _DT[dt],
+                                 _p(dt_bias), int(bool(delta_softplus)), _stream())
+    check(rc, "ss_scan_bwd_summary")
+    return g_start, dsum
+
+
+def ss_scan_carries(A, delta_sum, summ, init=None, reverse: bool = False):
+    """Compose P pieces' affine maps (piece-major ``delta_sum [P,B,D]``, ``summ [P,B,D,N]``)
+    -> ``carry [P,B,D,N]``: the state entering each piece (forward) or the carry arriving
+    at its end (``reverse``), starting from ``init`` (zeros when None)."""
+    lib = load()
+    P, B, D, N = summ.shape
+    dev = summ.device
+    _req(A, "A", (D, N), torch.float32, dev)
+    _req(delta_sum, "delta_sum", (P, B, D), torch.float32, dev)
+    _req(summ, "summ", (P, B, D, N), torch.float32, dev)
+    if init is not None:
+        _req(init, "init", (B, D, N), torch.float32, dev)
+    carry = torch.empty((P, B, D, N), device=dev, dtype=torch.float32)
+    rc = lib.ss_scan_carries(_p(A), _p(delta_sum), _p(summ), _p(init), _p(carry), P, B, D, N, int(bool(reverse)),
+                             _stream())
+    check(rc, "ss_scan_carries")
+    return carry
 
 
 def conv1d_causal_bwd(dout, x, w, dw=None, db=None, workspace=None):
