@@ -155,6 +155,33 @@ struct ActT<__nv_bfloat16> {
   }
 };
 
+// 8 consecutive activations as loaded (16 bytes of bf16, 32 of fp32) and their widening
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  using V = uint4;
+  static __device__ __forceinline__ V ld(const __nv_bfloat16* p) { return *reinterpret_cast<const uint4*>(p); }
+  static __device__ __forceinline__ V zero() { return make_uint4(0u, 0u, 0u, 0u); }
+  static __device__ __forceinline__ void wide(const V& v, float* o) {
+    o[0] = bf16_lo(v.x); o[1] = bf16_hi(v.x); o[2] = bf16_lo(v.y); o[3] = bf16_hi(v.y);
+    o[4] = bf16_lo(v.z); o[5] = bf16_hi(v.z); o[6] = bf16_lo(v.w); o[7] = bf16_hi(v.w);
+  }
+};
+template <>
+struct Raw8<float> {
+  struct V {
+    float4 a, b;
+  };
+  static __device__ __forceinline__ V ld(const float* p) {
+    return V{reinterpret_cast<const float4*>(p)[0], reinterpret_cast<const float4*>(p)[1]};
+  }
+  static __device__ __forceinline__ V zero() { return V{make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)}; }
+  static __device__ __forceinline__ void wide(const V& v, float* o) {
+    o[0] = v.a.x; o[1] = v.a.y; o[2] = v.a.z; o[3] = v.a.w; o[4] = v.b.x; o[5] = v.b.y; o[6] = v.b.z; o[7] = v.b.w;
+  }
+};
+
 // ---------------------------------------------------------------- smem / mbarrier / TMA
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -297,11 +324,42 @@ constexpr unsigned kErrTmaTimeout = 1u;
 // (loads issued four at a time, adds in that order), then the RG partial sums
 // are added y = 0..RG-1; deterministic run to run.  RG = 32 when the columns
 // alone give too few blocks to fill the GPU.
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with launch_dependent() may be scheduled while the kernel
+// before it in the stream is still running; it must call pdl_wait() before it
+// reads anything that kernel writes (the wait returns once that grid has
+// completed and its writes are visible; it returns at once for a kernel
+// launched the ordinary way).  pdl_trigger() in the kernel before lets the
+// dependent launch start early; without it the dependent starts when it exits.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+#ifndef SS_PDL
+#define SS_PDL 1
+#endif
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = SS_PDL;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 template <class Store, int RG>
 __global__ void __launch_bounds__(32 * RG) colsum_kernel(const float* __restrict__ part, long long ncols, int rows, Store st) {
   __shared__ float red[RG][33];
   const long long i = (long long)blockIdx.x * 32 + threadIdx.x;
   float acc = 0.f;
+  pdl_wait();  // the partials come from the kernel before
   if (i < ncols) {
     int g = threadIdx.y;
     for (; g + 3 * RG < rows; g += 4 * RG) {
@@ -328,10 +386,8 @@ template <class Store>
 inline cudaError_t colsum(const float* part, long long ncols, int rows, Store st, cudaStream_t s) {
   const long long blocks = (ncols + 31) / 32;
   if (blocks < 4ll * device_sm_count() && rows >= 64)
-    colsum_kernel<Store, 32><<<(unsigned)blocks, dim3(32, 32), 0, s>>>(part, ncols, rows, st);
-  else
-    colsum_kernel<Store, 8><<<(unsigned)blocks, dim3(32, 8), 0, s>>>(part, ncols, rows, st);
-  return cudaGetLastError();
+    return launch_dependent(colsum_kernel<Store, 32>, dim3((unsigned)blocks), dim3(32, 32), 0, s, part, ncols, rows, st);
+  return launch_dependent(colsum_kernel<Store, 8>, dim3((unsigned)blocks), dim3(32, 8), 0, s, part, ncols, rows, st);
 }
 
 }  // namespace ssk

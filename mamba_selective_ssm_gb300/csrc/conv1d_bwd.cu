@@ -14,9 +14,12 @@
 // K-1 halo steps per tile come from L2).
 //
 // conv1d_causal_silu_bwd takes the gradient after a SiLU on the conv output
-// instead: the x window then reaches K-1 steps ahead as well, so that each
-// incoming dout[t] is turned into g[t] = dout[t] * silu'(pre[t]), with
-// pre[t] = bias + sum_k w[k] x[t-(K-1)+k] recomputed from x and w.
+// instead: a thread walks the input steps t of its tile and K-1 beyond, turns
+// each incoming dout[t] into g[t] = dout[t] * silu'(pre[t]) with
+// pre[t] = bias + sum_k w[k] x[t-(K-1)+k] recomputed from the x window behind
+// t, and completes dx[t-(K-1)] from the last K values of g; the loads of four
+// steps are issued together.  The four-channel arithmetic runs as packed
+// f32x2 operations (two per step where scalar code takes four).
 #include "common.cuh"
 
 namespace {
@@ -36,22 +39,51 @@ __device__ __forceinline__ float4 ld_x4<__nv_bfloat16>(const __nv_bfloat16* p) {
   return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
 }
 
+// raw x vector of 4 channels as loaded (8 bytes for bf16, 16 for fp32) and its widening
+template <typename T>
+struct RawX4;
+template <>
+struct RawX4<float> {
+  using V = float4;
+  static __device__ __forceinline__ V ld(const float* p) { return *reinterpret_cast<const float4*>(p); }
+  static __device__ __forceinline__ float4 wide(V v) { return v; }
+  static __device__ __forceinline__ V zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+};
+template <>
+struct RawX4<__nv_bfloat16> {
+  using V = uint2;
+  static __device__ __forceinline__ V ld(const __nv_bfloat16* p) { return *reinterpret_cast<const uint2*>(p); }
+  static __device__ __forceinline__ float4 wide(V v) { return make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)); }
+  static __device__ __forceinline__ V zero() { return make_uint2(0u, 0u); }
+};
+
+// four-channel arithmetic as two packed f32x2 operations (the same roundings as four scalar ones)
 __device__ __forceinline__ float4 f4fma(float4 a, float4 b, float4 c) {
-  return make_float4(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y), fmaf(a.z, b.z, c.z), fmaf(a.w, b.w, c.w));
+  const float2 lo = fma2(f2(a.x, a.y), f2(b.x, b.y), f2(c.x, c.y));
+  const float2 hi = fma2(f2(a.z, a.w), f2(b.z, b.w), f2(c.z, c.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
-__device__ __forceinline__ float4 f4add(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
+  const float2 lo = add2(f2(a.x, a.y), f2(b.x, b.y)), hi = add2(f2(a.z, a.w), f2(b.z, b.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+// g * silu'(v) for two channels: sigmoid s = 1 / (1 + 2^(-v log2 e)), silu'(v) = s (1 + v (1 - s))
+__device__ __forceinline__ float2 gdsilu2(float2 g, float2 v) {
+  const float2 e = ex2_2(mul2(v, bc2(-kLog2e)));
+  const float2 den = add2(e, bc2(1.0f));
+  const float2 sg = f2(rcp(den.x), rcp(den.y));
+  const float2 t = fma2(v, fma2(sg, bc2(-1.0f), bc2(1.0f)), bc2(1.0f));
+  return mul2(g, mul2(sg, t));
+}
 __device__ __forceinline__ float4 f4z() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
-__device__ __forceinline__ float dsilu(float v) {
-  const float sg = sigmoid(v);
-  return sg * fmaf(v, 1.0f - sg, 1.0f);
-}
 
 template <int K, typename T, bool SILU>
 __global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __restrict__ dout, const T* __restrict__ x,
                                                              const float* __restrict__ w, const float* __restrict__ bias,
                                                              float* __restrict__ dx, float* __restrict__ ws, int B, int L,
                                                              int D) {
+  pdl_trigger();  // the column sum of the partials may launch now; it waits for this grid's end
   // Rows narrower than a CTA (D/4 < kCThreads channel quads) pack ipc items per
   // CTA step: thread slot `sub` takes every ipc-th item of its CTA row.
   const int cpr = D / 4;
@@ -75,43 +107,62 @@ __global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __r
     float4 pre = b4;
 #pragma unroll
     for (int k = 0; k < K; ++k) pre = f4fma(wk[k], xs[k], pre);
-    return make_float4(g.x * dsilu(pre.x), g.y * dsilu(pre.y), g.z * dsilu(pre.z), g.w * dsilu(pre.w));
+    const float2 lo = gdsilu2(f2(g.x, g.y), f2(pre.x, pre.y)), hi = gdsilu2(f2(g.z, g.w), f2(pre.z, pre.w));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
   };
 
   if (valid && SILU) {
+    // walk the input steps t = t0 .. t1+K-2: g[t] is formed once from the x window behind t, enters dw / db
+    // when t < t1, and completes dx[t-(K-1)] when that is in the tile; loads issued U steps at a time
+    constexpr int U = 4;  // loads issued together (8 spills at 128 registers; 2 slower)
+    using R = RawX4<T>;
     for (int bt = blockIdx.y * ipc + sub; bt < B * ntt; bt += gridDim.y * ipc) {
       const int b = bt / ntt, t0 = (bt % ntt) * kCTile;
       const int t1 = min(L, t0 + kCTile);
+      const int tend = t1 + K - 1, tl = min(L, tend);
       const float* g = dout + (size_t)b * L * D + d;
       const T* xb = x + (size_t)b * L * D + d;
-      float4 gw[K];          // gw[j] = g[s+j]
-      float4 xa[2 * K - 1];  // xa[j] = x[s-(K-1)+j]: K-1 steps behind to K-1 ahead
-#pragma unroll
-      for (int j = 0; j < 2 * K - 2; ++j) {
-        const int tx = t0 - (K - 1) + j;
-        xa[j + 1] = (tx >= 0 && tx < L) ? ld_x4(xb + (size_t)tx * D) : f4z();
-      }
+      float4 xw[K], gw[K];  // xw[k] = x[t-(K-1)+k], gw[j] = g[t-(K-1)+j]
 #pragma unroll
       for (int j = 0; j < K - 1; ++j) {
-        const int t = t0 + j;
-        gw[j + 1] = t < L ? gact(*reinterpret_cast<const float4*>(g + (size_t)t * D), &xa[j + 1]) : f4z();
+        const int tx = t0 - (K - 1) + j;
+        xw[j + 1] = tx >= 0 ? ld_x4(xb + (size_t)tx * D) : f4z();
+        gw[j + 1] = f4z();  // only ever combined into outputs before t0
       }
-#pragma unroll 8
-      for (int s = t0; s < t1; ++s) {
+      for (int tb = t0; tb < tend; tb += U) {
+        float4 gr[U];
+        typename R::V xr[U];
 #pragma unroll
-        for (int j = 0; j < 2 * K - 2; ++j) xa[j] = xa[j + 1];
+        for (int u = 0; u < U; ++u) {
+          const bool in = tb + u < tl;
+          gr[u] = in ? *reinterpret_cast<const float4*>(g + (size_t)(tb + u) * D) : f4z();
+          xr[u] = in ? R::ld(xb + (size_t)(tb + u) * D) : R::zero();
+        }
 #pragma unroll
-        for (int j = 0; j < K - 1; ++j) gw[j] = gw[j + 1];
-        const int tg = s + K - 1;
-        xa[2 * K - 2] = tg < L ? ld_x4(xb + (size_t)tg * D) : f4z();
-        gw[K - 1] = tg < L ? gact(*reinterpret_cast<const float4*>(g + (size_t)tg * D), &xa[K - 1]) : f4z();
-        float4 acc = f4z();
+        for (int u = 0; u < U; ++u) {
+          const int t = tb + u;
+          if (t < tend) {
 #pragma unroll
-        for (int j = 0; j < K; ++j) acc = f4fma(gw[j], wk[K - 1 - j], acc);
-        *reinterpret_cast<float4*>(dx + ((size_t)b * L + s) * D + d) = acc;
+            for (int j = 0; j < K - 1; ++j) {
+              xw[j] = xw[j + 1];
+              gw[j] = gw[j + 1];
+            }
+            xw[K - 1] = R::wide(xr[u]);
+            gw[K - 1] = gact(gr[u], xw);
+            if (t < t1) {
 #pragma unroll
-        for (int k = 0; k < K; ++k) dw[k] = f4fma(gw[0], xa[k], dw[k]);
-        db = f4add(db, gw[0]);
+              for (int k = 0; k < K; ++k) dw[k] = f4fma(gw[K - 1], xw[k], dw[k]);
+              db = f4add(db, gw[K - 1]);
+            }
+            const int s = t - (K - 1);
+            if (s >= t0) {
+              float4 acc = f4z();
+#pragma unroll
+              for (int j = 0; j < K; ++j) acc = f4fma(gw[j], wk[K - 1 - j], acc);
+              *reinterpret_cast<float4*>(dx + ((size_t)b * L + s) * D + d) = acc;
+            }
+          }
+        }
       }
     }
   } else if (valid) {

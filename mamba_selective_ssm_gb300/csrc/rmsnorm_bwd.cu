@@ -11,7 +11,8 @@
 // filled by untiled bulk copies (cp.async.bulk, one mbarrier per stage), so
 // up to nst rows of dy and x per CTA are in flight without holding registers
 // (rms_bwd_tma_kernel, rows of 2049 .. 8192 columns); rows of 257 .. 2048
-// columns go one warp per row (rms_bwd_warp_kernel, no block barrier per row);
+// columns are split over a CTA's threads, which walk the rows with the next
+// row's loads in flight and one barrier per row (rms_bwd_cols_kernel);
 // the register-prefetch form (rms_bwd_kernel, one row ahead) serves the
 // fixed-grid no-alloc entry point and rows too wide for two stages.  Per-CTA
 // dscale partials are added in fixed order by colsum_kernel.
@@ -40,6 +41,7 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_kernel(const T* __rest
                                                                  const float* __restrict__ scale,
                                                                  const float* __restrict__ rms, float* __restrict__ dx,
                                                                  float* __restrict__ ws, int rows, int dim) {
+  pdl_trigger();  // the column sum of the partials may launch now; it waits for this grid's end
   __shared__ float red[2][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
   float sc[VPT][8], acc[VPT][8], gy[VPT][8], xv[VPT][8], gyn[VPT][8], xvn[VPT][8];
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_tma_kernel(const T* __
                                                                      const float* __restrict__ scale,
                                                                      const float* __restrict__ rms, float* __restrict__ dx,
                                                                      float* __restrict__ ws, int rows, int dim, int nst) {
+  pdl_trigger();  // the column sum of the partials may launch now; it waits for this grid's end
   extern __shared__ __align__(128) unsigned char sm[];
   __shared__ float red[2][32];
   const uint32_t row_bytes = (uint32_t)dim * sizeof(T);
@@ -221,128 +224,6 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_bwd_tma_kernel(const T* __
   }
 }
 
-// Rows of 257 .. 2048 columns: one warp per row, no block barrier.  Lane l owns
-// the 8-column groups l, l + 32, ... (VPW of them), keeps scale and its dscale
-// partial sums in registers, and reads the row twice from its warp's ring of
-// shared-memory stages (bulk copies, one mbarrier per stage): once for the dot
-// product, reduced with shuffles, and once for dx.  The CTA's warps add their
-// dscale partials in fixed order at the end; a warp that gave up on a wait
-// contributes zeros (its outputs are invalid and ss_device_status reports it).
-constexpr int kRmsWarps = 4;
-
-template <typename T, int VPW>
-__global__ void __launch_bounds__(32 * kRmsWarps) rms_bwd_warp_kernel(const T* __restrict__ dy, const T* __restrict__ x,
-                                                                      const float* __restrict__ scale,
-                                                                      const float* __restrict__ rms,
-                                                                      float* __restrict__ dx, float* __restrict__ ws,
-                                                                      int rows, int dim, int nst) {
-  extern __shared__ __align__(128) unsigned char sm[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t row_bytes = (uint32_t)dim * sizeof(T);
-  T* buf = reinterpret_cast<T*>(sm) + (size_t)warp * nst * 2 * dim;  // this warp's [nst][dy | x][dim]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)kRmsWarps * nst * 2 * row_bytes) + warp * nst;
-  const long long nwarps = (long long)gridDim.x * kRmsWarps;
-  const long long gw = (long long)blockIdx.x * kRmsWarps + warp;
-  const int nk = gw < rows ? (int)((rows - gw + nwarps - 1) / nwarps) : 0;  // rows of this warp
-  auto issue = [&](int k) {  // lane 0; the stage's readers passed a warp sync
-    fence_proxy_async_smem();
-    const size_t r = (size_t)(gw + (long long)k * nwarps);
-    const int st = k % nst;
-    mbar_arrive_expect_tx(&full[st], 2 * row_bytes);
-    bulk_load(buf + (size_t)(2 * st) * dim, dy + r * dim, row_bytes, &full[st]);
-    bulk_load(buf + (size_t)(2 * st + 1) * dim, x + r * dim, row_bytes, &full[st]);
-  };
-  if (lane == 0) {
-    for (int st = 0; st < nst; ++st) mbar_init(&full[st], 1);
-    fence_barrier_init();
-    for (int k = 0; k < nst && k < nk; ++k) issue(k);
-  }
-  float sc[VPW][8], acc[VPW][8];
-#pragma unroll
-  for (int v = 0; v < VPW; ++v) {
-    const int c = (v * 32 + lane) * 8;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      sc[v][e] = c < dim ? scale[c + e] : 0.f;
-      acc[v][e] = 0.f;
-    }
-  }
-  __syncwarp();
-  const float inv_dim = 1.0f / (float)dim;
-  bool failed = false;
-  float rms_next = nk > 0 ? rms[gw] : 1.f;  // the row's rms, read one row ahead
-  for (int k = 0; k < nk; ++k) {
-    const long long r = gw + (long long)k * nwarps;
-    const int st = k % nst;
-    const float inv = 1.0f / rms_next;
-    if (k + 1 < nk) rms_next = rms[r + nwarps];
-    const bool ok = mbar_wait_bounded(&full[st], (k / nst) & 1, kWaitLimitNs);
-    if (__any_sync(0xffffffffu, !ok)) {
-      if (lane == 0) {
-        atomicOr(&g_rms_err, kErrTmaTimeout);
-        for (int k2 = k; k2 < k + nst && k2 < nk; ++k2) mbar_wait_bounded(&full[k2 % nst], (k2 / nst) & 1, 100000000ull);
-      }
-      failed = true;
-      break;
-    }
-    const T* g_s = buf + (size_t)(2 * st) * dim;
-    const T* x_s = buf + (size_t)(2 * st + 1) * dim;
-    float part = 0.f;
-#pragma unroll
-    for (int v = 0; v < VPW; ++v) {
-      const int c = (v * 32 + lane) * 8;
-      if (c < dim) {
-        float gv[8], xv[8];
-        ActT<T>::ld8(g_s + c, gv);
-        ActT<T>::ld8(x_s + c, xv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) part = fmaf(gv[e] * sc[v][e], xv[e], part);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    const float kk = part * inv * inv * inv_dim;
-#pragma unroll
-    for (int v = 0; v < VPW; ++v) {
-      const int c = (v * 32 + lane) * 8;
-      if (c < dim) {
-        float gv[8], xv[8], o[8];
-        ActT<T>::ld8(g_s + c, gv);
-        ActT<T>::ld8(x_s + c, xv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          o[e] = inv * (sc[v][e] * gv[e]) - inv * (xv[e] * kk);
-          acc[v][e] = fmaf(gv[e] * xv[e], inv, acc[v][e]);
-        }
-        ActT<float>::st8(dx + (size_t)r * dim + c, o);
-      }
-    }
-    __syncwarp();
-    if (lane == 0 && k + nst < nk) issue(k + nst);
-  }
-  if (failed) {
-#pragma unroll
-    for (int v = 0; v < VPW; ++v)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[v][e] = 0.f;
-  }
-  // the CTA's dscale partial row: the warps' sums added in warp order (the stages are free now)
-  __syncthreads();
-  float* red = reinterpret_cast<float*>(sm);  // [kRmsWarps][dim], within the stage buffers
-#pragma unroll
-  for (int v = 0; v < VPW; ++v) {
-    const int c = (v * 32 + lane) * 8;
-    if (c < dim) ActT<float>::st8(red + (size_t)warp * dim + c, acc[v]);
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c < dim; c += 32 * kRmsWarps) {
-    float a = red[c];
-#pragma unroll
-    for (int w = 1; w < kRmsWarps; ++w) a += red[(size_t)w * dim + c];
-    ws[(size_t)blockIdx.x * dim + c] = a;
-  }
-}
-
 // Rows of at most 256 columns: G lanes per row (one 8-column group each), 32/G
 // rows per warp, the dot product reduced by shuffles inside each G-lane
 // segment, no block barrier per row.  The dscale partials of the CTA's
@@ -352,6 +233,7 @@ __global__ void __launch_bounds__(256) rms_bwd_small_kernel(const T* __restrict_
                                                             const float* __restrict__ scale, const float* __restrict__ rms,
                                                             float* __restrict__ dx, float* __restrict__ ws, int rows,
                                                             int dim) {
+  pdl_trigger();  // the column sum of the partials may launch now; it waits for this grid's end
   constexpr int R = 32 / G;
   __shared__ float red[8 * R][G * 8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
@@ -489,37 +371,119 @@ int rms_tma_launch(const void* dy, const void* x, const float* scale, const floa
   return run(rms_bwd_tma_kernel<T, 1>);
 }
 
-// The warp-per-row form: up to 4 stages per warp within ~100 KB per CTA, as many CTAs as fit (at most the
-// workspace's partial rows); the dscale partial rows are added by colsum_kernel.
-template <typename T>
-int rms_warp_launch(const void* dy, const void* x, const float* scale, const float* rms, float* dx, float* dscale,
-                    int rows, int dim, float* ws, const RmsPlan& pl, cudaStream_t s) {
-  const size_t pair = (size_t)2 * dim * sizeof(T);
-  int nst = (int)((100u * 1024u) / (kRmsWarps * pair));
-  if (nst > 4) nst = 4;
-  if (nst < 2) nst = 2;
-  size_t smem = (size_t)kRmsWarps * nst * pair + (size_t)kRmsWarps * nst * sizeof(uint64_t);
-  if (smem < (size_t)kRmsWarps * dim * sizeof(float)) smem = (size_t)kRmsWarps * dim * sizeof(float);  // the final sum
-  const T* g = static_cast<const T*>(dy);
-  const T* xx = static_cast<const T*>(x);
-  auto run = [&](auto kern) -> int {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return SS_ERR_CUDA;
-    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-    const int per_sm = resident_ctas(kern, 32 * kRmsWarps, smem);
-    if (per_sm < 1) return SS_ERR_CUDA;
-    long long grid = (long long)per_sm * device_sm_count();
-    const long long need = ((long long)rows + kRmsWarps - 1) / kRmsWarps;
-    if (grid > need) grid = need;
-    if (grid > pl.grid) grid = pl.grid;  // the workspace holds pl.grid partial rows
-    if (grid < 1) grid = 1;
-    kern<<<(int)grid, 32 * kRmsWarps, smem, s>>>(g, xx, scale, rms, dx, ws, rows, dim, nst);
-    if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
-    return colsum(ws, dim, (int)grid, AddTo{dscale}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+// Rows of 257 .. 2048 columns, column-split: the CTA's threads share the
+// columns (8 each, one 16- or 32-byte vector of a row) and walk groups of R
+// rows.  A thread loads its columns of the R rows' dy and x at once; each row's
+// dot product is summed over the thread's 8 columns, across the warp by
+// shuffles and across the warps through shared memory in warp order (one
+// barrier per R rows, parity-buffered); every thread keeps its columns' dscale
+// partial in registers over all the rows it visits.
+template <typename T, int R, bool PF>
+__global__ void __launch_bounds__(256) rms_bwd_cols_kernel(const T* __restrict__ dy, const T* __restrict__ x,
+                                                           const float* __restrict__ scale, const float* __restrict__ rms,
+                                                           float* __restrict__ dx, float* __restrict__ ws, int rows,
+                                                           int dim) {
+  pdl_trigger();  // the column sum of the partials may launch now; it waits for this grid's end
+  using Rw = Raw8<T>;
+  using Buf = typename Rw::V[R];
+  __shared__ float part[2][R][8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = (int)blockDim.x >> 5;
+  const int c = (int)threadIdx.x * 8;
+  const bool cv = c < dim;
+  float sc[8], acc[8];
+  {
+    const float4 s0 = cv ? __ldg(reinterpret_cast<const float4*>(scale + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 s1 = cv ? __ldg(reinterpret_cast<const float4*>(scale + c + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    sc[0] = s0.x; sc[1] = s0.y; sc[2] = s0.z; sc[3] = s0.w; sc[4] = s1.x; sc[5] = s1.y; sc[6] = s1.z; sc[7] = s1.w;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  const float inv_dim = 1.0f / (float)dim;
+  const long long step = (long long)gridDim.x * R;
+  auto load = [&](Buf& gr, Buf& xr, long long r0) {
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const long long r = r0 + i;
+      const bool ok = cv && r < rows;
+      gr[i] = ok ? Rw::ld(dy + (size_t)r * dim + c) : Rw::zero();
+      xr[i] = ok ? Rw::ld(x + (size_t)r * dim + c) : Rw::zero();
+    }
   };
-  const int vpw = (dim + 255) / 256;
-  if (vpw <= 2) return run(rms_bwd_warp_kernel<T, 2>);
-  if (vpw <= 4) return run(rms_bwd_warp_kernel<T, 4>);
-  return run(rms_bwd_warp_kernel<T, 8>);
+  int par = 0;
+  auto finish = [&](const Buf& gr, const Buf& xr, long long r0) {
+    float rinv[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) rinv[i] = r0 + i < rows ? 1.0f / __ldg(rms + r0 + i) : 0.f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      float gv[8], xv[8];
+      Rw::wide(gr[i], gv);
+      Rw::wide(xr[i], xv);
+      float a = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a = fmaf(gv[e] * sc[e], xv[e], a);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if (lane == 0) part[par][i][warp] = a;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const long long r = r0 + i;
+      if (r < rows && cv) {
+        float dot = part[par][i][0];
+        for (int w = 1; w < nwarp; ++w) dot += part[par][i][w];
+        const float inv = rinv[i];
+        const float kk = dot * inv * inv * inv_dim;
+        float gv[8], xv[8], o[8];
+        Rw::wide(gr[i], gv);
+        Rw::wide(xr[i], xv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          o[e] = inv * (sc[e] * gv[e]) - inv * (xv[e] * kk);
+          acc[e] = fmaf(gv[e] * xv[e], inv, acc[e]);
+        }
+        ActT<float>::st8(dx + (size_t)r * dim + c, o);
+      }
+    }
+    par ^= 1;
+  };
+  Buf ga, xa, gb, xb;
+  long long r0 = (long long)blockIdx.x * R;
+  if constexpr (!PF) {
+    for (; r0 < rows; r0 += step) {
+      load(ga, xa, r0);
+      finish(ga, xa, r0);
+    }
+  } else {
+    if (r0 < rows) load(ga, xa, r0);
+    for (; r0 < rows; r0 += 2 * step) {
+      if (r0 + step < rows) load(gb, xb, r0 + step);
+      finish(ga, xa, r0);
+      if (r0 + step >= rows) break;
+      if (r0 + 2 * step < rows) load(ga, xa, r0 + 2 * step);
+      finish(gb, xb, r0 + step);
+    }
+  }
+  if (cv) ActT<float>::st8(ws + (size_t)blockIdx.x * dim + c, acc);
+}
+
+template <typename T>
+int rms_cols_launch(const void* dy, const void* x, const float* scale, const float* rms, float* dx, float* dscale,
+                    int rows, int dim, float* ws, const RmsPlan& pl, cudaStream_t s) {
+  constexpr int R = 1;  // one row per step, the next row's loads in flight (measured best of 1, 2, 4, 8 rows)
+  auto kern = rms_bwd_cols_kernel<T, R, true>;
+  const int threads = (dim / 8 + 31) / 32 * 32;
+  const int per_sm = resident_ctas(kern, threads, 0);
+  if (per_sm < 1) return SS_ERR_CUDA;
+  long long grid = (long long)per_sm * device_sm_count();
+  const long long need = ((long long)rows + R - 1) / R;
+  if (grid > need) grid = need;
+  if (grid > pl.grid) grid = pl.grid;  // the workspace holds pl.grid partial rows
+  if (grid < 1) grid = 1;
+  kern<<<(int)grid, threads, 0, s>>>(static_cast<const T*>(dy), static_cast<const T*>(x), scale, rms, dx, ws, rows, dim);
+  if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+  return colsum(ws, dim, (int)grid, AddTo{dscale}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 template <typename T>
@@ -558,9 +522,9 @@ extern "C" int rmsnorm_bwd(const void* dy, const void* x, const float* scale, co
     if (dtype == SS_F32) return rms_small_dispatch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
     return rms_small_dispatch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
   }
-  if (dim <= 2048) {  // one warp per row
-    if (dtype == SS_F32) return rms_warp_launch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
-    return rms_warp_launch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+  if (dim <= 2048) {  // columns split over a CTA
+    if (dtype == SS_F32) return rms_cols_launch<float>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
+    return rms_cols_launch<__nv_bfloat16>(dy, x, scale, rms, dx, dscale, rows, dim, ws, pl, s);
   }
   const int nst = rms_tma_stages(dim, dtype == SS_F32 ? 4 : 2);
   if (nst > 0 && pl.vpt == 1) {  // dim <= 8192 and two stages fit

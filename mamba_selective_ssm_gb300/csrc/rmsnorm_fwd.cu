@@ -7,9 +7,10 @@
 // 8 consecutive columns; the row's sum of squares is reduced with warp
 // shuffles and one shared-memory exchange whose buffer alternates with the
 // row parity; y is written in the input dtype (bf16 rounded to nearest even)
-// and rms_r in fp32.  Rows of 257 .. 2048 columns go one warp per row through
-// a per-warp ring of bulk-copied stages (rms_fwd_warp_kernel, no block barrier
-// per row); rows of at most 8192 columns arrive through a per-CTA ring of
+// and rms_r in fp32.  Rows of 257 .. 2048 columns (1024 for fp32) go one warp
+// per row with the row in registers (rms_fwd_reg_kernel); fp32 rows of 1025 ..
+// 2048 columns one warp per row through a per-warp ring of bulk-copied stages
+// (rms_fwd_warp_kernel); rows of at most 8192 columns arrive through a per-CTA ring of
 // shared-memory stages filled by untiled bulk copies (rms_fwd_tma_kernel);
 // wider rows use the register-prefetch form (one row ahead).
 #include "common.cuh"
@@ -277,6 +278,83 @@ int rms_fwd_warp_launch(const void* x, const float* scale, float eps, void* y, f
   return run(rms_fwd_warp_kernel<T, 8>);
 }
 
+// Rows of 257 .. 2048 columns (bf16; 1024 for fp32), held in registers: one
+// warp per row, lane l owning the 8-column groups l, l + 32, ... (VPW of
+// them), all of a row's loads issued together.  The warps of a CTA walk rows
+// w, w + W, ... and the CTA stages scale in shared memory once (a lane reads
+// its 8 values as two 16-byte words that neighbouring lanes' words follow, so
+// the reads are conflict-free); reading scale from global memory per row
+// measured 3 us slower on the 1.4B layer's [8192, 2048] rows, and a second row
+// buffer per warp (loads of the next row in flight) no faster.
+constexpr int kRmsRegWarps = 8;
+
+template <typename T, int VPW>
+__global__ void __launch_bounds__(32 * kRmsRegWarps, VPW >= 8 ? 3 : 4) rms_fwd_reg_kernel(const T* __restrict__ x,
+                                                                        const float* __restrict__ scale, float eps,
+                                                                        T* __restrict__ y, float* __restrict__ rms,
+                                                                        int rows, int dim) {
+  using R = Raw8<T>;
+  extern __shared__ float4 ssc[];  // [2][dim / 8]: group g's first four values at g, last four at dim/8 + g
+  const int ng = dim / 8;
+  for (int i = threadIdx.x; i < ng; i += blockDim.x) {
+    ssc[i] = __ldg(reinterpret_cast<const float4*>(scale) + 2 * i);
+    ssc[ng + i] = __ldg(reinterpret_cast<const float4*>(scale) + 2 * i + 1);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const long long nw = (long long)gridDim.x * kRmsRegWarps;
+  const float inv_dim = 1.0f / (float)dim;
+  for (long long r = (long long)blockIdx.x * kRmsRegWarps + (threadIdx.x >> 5); r < rows; r += nw) {
+    typename R::V b[VPW];
+#pragma unroll
+    for (int v = 0; v < VPW; ++v) {
+      const int c = (v * 32 + lane) * 8;
+      b[v] = c < dim ? R::ld(x + (size_t)r * dim + c) : R::zero();
+    }
+    float part = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPW; ++v) {
+      float xv[8];
+      R::wide(b[v], xv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) part = fmaf(xv[e], xv[e], part);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    const float rr = sqrtf(fmaf(part, inv_dim, eps));
+    const float inv = 1.0f / rr;
+    if (lane == 0 && rms != nullptr) rms[r] = rr;
+#pragma unroll
+    for (int v = 0; v < VPW; ++v) {
+      const int c = (v * 32 + lane) * 8;
+      if (c < dim) {
+        float xv[8], o[8];
+        R::wide(b[v], xv);
+        const float4 s0 = ssc[v * 32 + lane], s1 = ssc[ng + v * 32 + lane];
+        const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = (xv[e] * sc[e]) * inv;
+        ActT<T>::st8(y + (size_t)r * dim + c, o);
+      }
+    }
+  }
+}
+
+template <typename T, int VPW>
+int rms_fwd_reg_launch(const void* x, const float* scale, float eps, void* y, float* rms, int rows, int dim,
+                       cudaStream_t s) {
+  auto kern = rms_fwd_reg_kernel<T, VPW>;
+  const size_t smem = (size_t)dim * sizeof(float);
+  const int per_sm = resident_ctas(kern, 32 * kRmsRegWarps, smem);
+  if (per_sm < 1) return SS_ERR_CUDA;
+  long long grid = (long long)per_sm * device_sm_count();
+  const long long need = ((long long)rows + kRmsRegWarps - 1) / kRmsRegWarps;
+  if (grid > need) grid = need;
+  kern<<<(int)grid, 32 * kRmsRegWarps, smem, s>>>(static_cast<const T*>(x), scale, eps, static_cast<T*>(y), rms, rows,
+                                                  dim);
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
 // Rows of at most 256 columns: G lanes per row (one 8-column group each), 32/G
 // rows per warp, the sum of squares reduced by shuffles inside each G-lane
 // segment, no block barrier per row.
@@ -352,6 +430,12 @@ int rms_fwd_launch(const void* x, const float* scale, float eps, void* y, float*
     if (groups <= 8) return rms_fwd_small_launch<T, 8>(x, scale, eps, y, rms, rows, dim, s);
     if (groups <= 16) return rms_fwd_small_launch<T, 16>(x, scale, eps, y, rms, rows, dim, s);
     return rms_fwd_small_launch<T, 32>(x, scale, eps, y, rms, rows, dim, s);
+  }
+  constexpr int kRegMaxGroups = sizeof(T) == 2 ? 256 : 128;  // rows held in registers: 64 columns a lane (bf16)
+  if (groups <= kRegMaxGroups) {
+    if (groups <= 64) return rms_fwd_reg_launch<T, 2>(x, scale, eps, y, rms, rows, dim, s);
+    if (groups <= 128) return rms_fwd_reg_launch<T, 4>(x, scale, eps, y, rms, rows, dim, s);
+    if constexpr (sizeof(T) == 2) return rms_fwd_reg_launch<T, 8>(x, scale, eps, y, rms, rows, dim, s);
   }
   if (groups <= 256) return rms_fwd_warp_launch<T>(x, scale, eps, y, rms, rows, dim, s);  // one warp per row
   if (groups <= 1024) {  // one 8-column group per thread: the bulk-copy ring, up to 16 rows or ~100 KB per CTA

@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BwdSmem<T, N, NSTG, DT>& S = *reinterpret_cast<BwdSmem<T, N, NSTG, DT>*>(smem_raw);
 
+  pdl_trigger();  // the reduction of the partials may launch now; it waits for this grid's end
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ng = lane % G::NG, cg = lane / G::NG;
   const int dl = warp * G::WC + cg * 2;
@@ -781,6 +782,7 @@ __global__ void __launch_bounds__(256) ss_bwd_reduce_kernel(const float* __restr
                                                             long long nBC, int ndt, int nblk_bc,
                                                             const float* __restrict__ ws_dAD, long long nAD, int rows,
                                                             DADStore st) {
+  pdl_wait();  // the partials come from the backward kernel before
   if ((int)blockIdx.x < nblk_bc) {
     for (long long i = blockIdx.x * 256ll + threadIdx.x; i < nBC; i += (long long)nblk_bc * 256) {
       float acc = 0.f;
@@ -937,9 +939,10 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
   if (blk_bc > 8192) blk_bc = 8192;
   const long long nA = (long long)p.D * N, nAD = nA + 2ll * p.D;
   const long long blk_ad = (nAD + 31) / 32;
-  ss_bwd_reduce_kernel<N><<<(unsigned)(blk_bc + blk_ad), 256, 0, stream>>>(
-      p.ws_dBC, dB, dC, nBC, pl.ndt, (int)blk_bc, p.ws_dAD, nAD, rows, DADStore{dA, dD, p.d_dt_bias, nA, p.D});
-  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  const cudaError_t err = launch_dependent(ss_bwd_reduce_kernel<N>, dim3((unsigned)(blk_bc + blk_ad)), dim3(256), 0, stream,
+                                         (const float*)p.ws_dBC, dB, dC, nBC, pl.ndt, (int)blk_bc, (const float*)p.ws_dAD,
+                                         nAD, rows, DADStore{dA, dD, p.d_dt_bias, nA, p.D});
+  return err == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 // the discretisation of delta is a template switch, so the plain scan carries none of it
