@@ -44,6 +44,12 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip timing the kernels next to the hot path")
     ap.add_argument("--no-others", action="store_true", help="skip timing the scan on the other workloads")
+    ap.add_argument("--profile", choices=["scan", "side"], default=None,
+                    help="only run the scan (or the conv1d / RMSNorm kernels) a few times on seeded device tensors, "
+                         "for a profiler to capture; prints nothing but 'ok'")
+    ap.add_argument("--B", type=int, default=None, help="--profile: batch rows (default: the workload's)")
+    ap.add_argument("--L", type=int, default=None, help="--profile: sequence length (default: the workload's)")
+    ap.add_argument("--iters", type=int, default=4, help="--profile: calls of each kernel")
     return ap.parse_args()
 
 
@@ -343,8 +349,52 @@ def time_scan_workload(wl, dev, peak, iters=10, warmup=3):
     return res
 
 
+def profile_run(args):
+    """The scan forward + backward (or conv1d fwd/bwd and RMSNorm fwd/bwd) on seeded device tensors of the
+    workload's shape (B and L overridable), args.iters times: a fixed, short launch sequence to profile."""
+    import torch
+
+    import mamba_selective_ssm_gb300 as ss
+    from workloads import get_config
+
+    ss.build()
+    wl = get_config(args.workload)
+    B, L = args.B or wl.B, args.L or wl.L
+    D, N, H, K = wl.D, wl.N, wl.d_model, wl.d_conv
+    dev = torch.device("cuda", 0)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    g = torch.Generator(device=dev).manual_seed(0)
+    rn = lambda *sh: torch.randn(*sh, device=dev, generator=g)
+    if args.profile == "scan":
+        x, z, dy = rn(B, L, D).to(tdt), rn(B, L, D).to(tdt), rn(B, L, D).to(tdt)
+        delta = (0.001 + 0.099 * torch.rand(B, L, D, device=dev, generator=g)).to(tdt)
+        Bm, Cm = rn(B, L, N).to(tdt), rn(B, L, N).to(tdt)
+        A = (-(torch.arange(N, device=dev) + 1.0)).repeat(D, 1).contiguous()
+        Dv = torch.ones(D, device=dev)
+        for _ in range(args.iters):
+            y, ck, _ = ss.ss_scan_fwd(x, delta, A, Bm, Cm, Dv, z, chunk=wl.chunk)
+            ss.ss_scan_bwd(x, delta, A, Bm, Cm, Dv, z, ck, dy, chunk=wl.chunk)
+    else:
+        x, dout = rn(B, L, D).to(tdt), rn(B, L, D)
+        w, bias = 0.5 * rn(D, K), 0.1 * rn(D)
+        rx, rdy = rn(B * L, H).to(tdt), rn(B * L, H).to(tdt)
+        sc = 1 + 0.1 * rn(H)
+        _, rms = ss.rmsnorm_fwd(rx, sc, 1e-5)
+        for _ in range(args.iters):
+            ss.rmsnorm_bwd(rdy, rx, sc, rms)
+            ss.rmsnorm_fwd(rx, sc, 1e-5)
+            ss.conv1d_causal_fwd(x, w, bias, silu=True)
+            ss.conv1d_causal_silu_bwd(dout, x, w, bias)
+            ss.conv1d_causal_bwd(dout, x, w)
+    torch.cuda.synchronize(dev)
+    print("ok")
+
+
 def main():
     args = parse()
+    if args.profile:
+        profile_run(args)
+        return
     if args.impl == "reference":
         run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
