@@ -230,3 +230,41 @@ def test_abi_is_usable_from_plain_c(lib, tmp_path):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_shard_entry_points_validation(lib):
+    """The sequence-sharding calls reject bad arguments on the host before any launch."""
+    from mamba_selective_ssm_gb300 import _capi as c
+    p = [_fake(0x50000 + 256 * i) for i in range(7)]
+    fs = lambda ptrs=p[:6], B=2, L=64, D=16, N=4, dt=c.SS_F32: lib.ss_scan_fwd_summary(*ptrs, B, L, D, N, dt, None, 0, None)
+    q = list(p[:6])
+    q[4] = None  # h_end
+    assert fs(q) == c.SS_ERR_NULL
+    assert fs(N=5) == c.SS_ERR_UNSUPPORTED
+    assert fs(dt=4) == c.SS_ERR_UNSUPPORTED
+    assert fs(B=0) == c.SS_ERR_DIM
+    assert fs(D=12) == c.SS_ERR_ALIGN
+    q = list(p[:6])
+    q[1] = _fake(0x50004)
+    assert fs(q) == c.SS_ERR_ALIGN
+    bs = lambda ptrs=p, B=2, L=64, D=16, N=16, dt=c.SS_BF16: lib.ss_scan_bwd_summary(*ptrs, B, L, D, N, dt, None, 1, None)
+    q = list(p)
+    q[4] = None  # dy
+    assert bs(q) == c.SS_ERR_NULL
+    assert bs(N=2) == c.SS_ERR_UNSUPPORTED
+    assert bs(L=-3) == c.SS_ERR_DIM
+    assert bs(D=20) == c.SS_ERR_ALIGN
+    q = list(p)
+    q[5] = _fake(0x50008)  # g_start
+    assert bs(q) == c.SS_ERR_ALIGN
+    r = [_fake(0x60000 + 256 * i) for i in range(5)]
+    car = lambda ptrs=r, P=4, B=2, D=16, N=16: lib.ss_scan_carries(*ptrs, P, B, D, N, 0, None)
+    q = list(r)
+    q[0] = None  # A
+    assert car(q) == c.SS_ERR_NULL
+    q = list(r)
+    q[4] = None  # carry
+    assert car(q) == c.SS_ERR_NULL
+    assert car(P=0) == c.SS_ERR_DIM
+    assert car(B=0) == c.SS_ERR_DIM
+    assert car(P=65) == c.SS_ERR_UNSUPPORTED
