@@ -27,6 +27,7 @@ namespace {
 using namespace ssk;
 
 constexpr int kCTile = 16;     // time steps per tile (short tiles: the (batch row, tile) items spread evenly over the CTAs)
+constexpr int kCTileSilu = 24;  // the SiLU-fused form recomputes K-1 steps of g per tile (16: 84 us, 24: 81, 32: 82)
 constexpr int kCThreads = 128;  // threads per CTA: 512 channels
 
 template <typename T>
@@ -91,7 +92,8 @@ __global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __r
   const int sub = cpr >= kCThreads ? 0 : (int)threadIdx.x / cpr;
   const int d = (cpr >= kCThreads ? (int)(blockIdx.x * kCThreads + threadIdx.x) : (int)threadIdx.x % cpr) * 4;
   const bool valid = d < D && sub < ipc;  // D % 8 == 0, so all four channels are in range
-  const int ntt = (L + kCTile - 1) / kCTile;
+  constexpr int TILE = SILU ? kCTileSilu : kCTile;
+  const int ntt = (L + TILE - 1) / TILE;
   float4 wk[K];  // wk[k] = w[d..d+3, k]
 #pragma unroll
   for (int k = 0; k < K; ++k)
@@ -117,8 +119,8 @@ __global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __r
     constexpr int U = 4;  // loads issued together (8 spills at 128 registers; 2 slower)
     using R = RawX4<T>;
     for (int bt = blockIdx.y * ipc + sub; bt < B * ntt; bt += gridDim.y * ipc) {
-      const int b = bt / ntt, t0 = (bt % ntt) * kCTile;
-      const int t1 = min(L, t0 + kCTile);
+      const int b = bt / ntt, t0 = (bt % ntt) * TILE;
+      const int t1 = min(L, t0 + TILE);
       const int tend = t1 + K - 1, tl = min(L, tend);
       const float* g = dout + (size_t)b * L * D + d;
       const T* xb = x + (size_t)b * L * D + d;
@@ -167,8 +169,8 @@ __global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __r
     }
   } else if (valid) {
     for (int bt = blockIdx.y * ipc + sub; bt < B * ntt; bt += gridDim.y * ipc) {
-      const int b = bt / ntt, t0 = (bt % ntt) * kCTile;
-      const int t1 = min(L, t0 + kCTile);
+      const int b = bt / ntt, t0 = (bt % ntt) * TILE;
+      const int t1 = min(L, t0 + TILE);
       const float* g = dout + (size_t)b * L * D + d;
       const T* xb = x + (size_t)b * L * D + d;
       float4 gw[K], xw[K];  // gw[j] = dout[s+j], xw[k] = x[s-(K-1)+k]
