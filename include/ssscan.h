@@ -375,7 +375,9 @@ int ss_count_nonfinite(const void* p, size_t n, int dtype, unsigned long long* c
  * ss_device_status — synchronises `stream`, then reads and clears the
  * library's device-side error word.  Returns SS_OK, or SS_ERR_DEVICE when a
  * kernel gave up on a bounded wait for its own asynchronous copies since the
- * last call (its outputs are then invalid), or SS_ERR_CUDA.
+ * last call (its overwritten outputs are then invalid; the CTAs that gave up
+ * add zero to the accumulated gradients dA, dD, d_dt_bias, dw, db, dscale),
+ * or SS_ERR_CUDA.
  */
 int ss_device_status(void* stream);
 

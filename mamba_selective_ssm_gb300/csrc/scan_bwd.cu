@@ -729,7 +729,12 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
   __syncthreads();
   tc_fence_after_sync();
   if (warp == 0 && !direct) tmem_dealloc(S.tmem_base, p.tcols);
-  if (failed) return;
+  if (failed) {  // a CTA that gave up on a wait adds nothing to the accumulated gradients
+#pragma unroll
+    for (int j = 0; j < 2; ++j) dA2[j][0] = dA2[j][1] = f2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dDacc[e] = dTacc[e] = 0.f;
+  }
 
   // per-CTA partials of dA, dD and d dt_bias (summed over this CTA's batch rows)
   float* row = p.ws_dAD + (size_t)blockIdx.y * p.D * (N + 2);
