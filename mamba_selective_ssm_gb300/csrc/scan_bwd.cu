@@ -120,22 +120,35 @@ struct BwdSumSmem {
   alignas(8) uint64_t full[NSTG];
 };
 
-// Segment summaries for segments 1 .. P-1: the adjoint each carries out of its
-// first step when the carry entering its last step is zero, and its sum of
-// delta.  CTA = (channel tile, (batch row, segment)); tiles walked last to first.
+// Summary-kernel geometry: one channel x 4 states per thread (the summary keeps
+// no per-step shares, so its threads can be half as wide as the main kernel's
+// and the segments get twice the warps), lane = ng * CPW + c so that the lanes
+// reading one state quad of C_t are consecutive.
+template <int N, int DT>
+struct GeoS {
+  static constexpr int NG = N / 4;      // lanes per channel
+  static constexpr int CPW = 32 / NG;   // channels per warp
+  static constexpr int W = DT / CPW;    // warps per CTA
+  static constexpr int NT = 32 * W;
+  static_assert(W >= 1 && DT % CPW == 0, "a CTA holds whole warps");
+};
+
+// Segment summaries: for each segment the adjoint it carries out of its first
+// step when the carry entering its last step is zero, and its sum of delta.
+// CTA = (channel tile, (batch row, segment)); tiles walked last to first.
 template <int N, typename T, int NSTG, int DT, bool FUSE>
-__global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const BwdParams p,
-                                                                       const __grid_constant__ CUtensorMap tm_dlt,
-                                                                       const __grid_constant__ CUtensorMap tm_z,
-                                                                       const __grid_constant__ CUtensorMap tm_dy,
-                                                                       const __grid_constant__ CUtensorMap tm_C) {
-  using G = Geo<N, DT>;
+__global__ void __launch_bounds__(GeoS<N, DT>::NT) scan_bwd_summary_kernel(const BwdParams p,
+                                                                        const __grid_constant__ CUtensorMap tm_dlt,
+                                                                        const __grid_constant__ CUtensorMap tm_z,
+                                                                        const __grid_constant__ CUtensorMap tm_dy,
+                                                                        const __grid_constant__ CUtensorMap tm_C) {
+  using G = GeoS<N, DT>;
   using AT = ActT<T>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BwdSumSmem<T, N, NSTG, DT>& S = *reinterpret_cast<BwdSumSmem<T, N, NSTG, DT>*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ng = lane % G::NG, cg = lane / G::NG;
-  const int dl = warp * G::WC + cg * 2;
+  const int ng = lane / G::CPW, c = lane % G::CPW;
+  const int dl = warp * G::CPW + c;
   const int d0 = blockIdx.x * DT;
   const int dg = d0 + dl;
   const bool dvalid = dg < p.D;
@@ -146,14 +159,12 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
   const int nitems = gte - gtb;
   constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
   constexpr uint32_t kStageBytes = 3 * kActBytes + kTT * N * AT::kBytes;
-  float2 Ap[2][2];
+  float2 Ap[2];
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const float* a = p.A + (size_t)(dvalid ? dg + j : 0) * N + n0 + 2 * q;
-      Ap[j][q] = dvalid ? f2(a[0] * kLog2e, a[1] * kLog2e) : f2(0.f, 0.f);
-    }
+  for (int q = 0; q < 2; ++q) {
+    const float* a = p.A + (size_t)(dvalid ? dg : 0) * N + n0 + 2 * q;
+    Ap[q] = dvalid ? f2(a[0] * kLog2e, a[1] * kLog2e) : f2(0.f, 0.f);
+  }
   auto issue = [&](int k) {
     fence_proxy_async_smem();  // the slot's earlier readers passed a barrier before this call
     const int slot = k % NSTG, t0 = (gte - 1 - k) * kTT;
@@ -163,7 +174,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
     tma_load_3d(S.dy[slot], &tm_dy, &S.full[slot], d0, t0, b);
     tma_load_2d(S.Cm[slot], &tm_C, &S.full[slot], t0 * N, b);
   };
-  for (int c = tid; c < DT; c += G::NT) S.bias_s[c] = (p.dt_bias != nullptr && d0 + c < p.D) ? p.dt_bias[d0 + c] : 0.f;
+  for (int cc = tid; cc < DT; cc += G::NT) S.bias_s[cc] = (p.dt_bias != nullptr && d0 + cc < p.D) ? p.dt_bias[d0 + cc] : 0.f;
   if (tid == 0) {
     prefetch_tmap(&tm_dlt); prefetch_tmap(&tm_z); prefetch_tmap(&tm_dy); prefetch_tmap(&tm_C);
     for (int st = 0; st < NSTG; ++st) mbar_init(&S.full[st], 1);
@@ -171,10 +182,8 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
     for (int k = 0; k < NSTG && k < nitems; ++k) issue(k);
   }
   __syncthreads();
-  float2 ga[2][2];
-  float dsum[2] = {0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < 2; ++j) ga[j][0] = ga[j][1] = f2(0.f, 0.f);
+  float2 ga[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+  float dsum = 0.f;
   for (int k = 0; k < nitems; ++k) {
     const int slot = k % NSTG;
     bool ok = true;
@@ -210,28 +219,20 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_summary_kernel(const 
     if (tid == 0 && k + NSTG < nitems) issue(k + NSTG);  // the slot is widened: refill it
 #pragma unroll
     for (int r = kTT - 1; r >= 0; --r) {
-      const float2 dd = *reinterpret_cast<const float2*>(&S.dlt_f[r * DT + dl]);
-      const float2 gg = *reinterpret_cast<const float2*>(&S.ds_f[r * DT + dl]);
+      const float dj = S.dlt_f[r * DT + dl];
+      const float2 gj = bc2(S.ds_f[r * DT + dl]);
       const float4 Cv = *reinterpret_cast<const float4*>(&S.C_f[r * N + n0]);
-      const float2 C01 = f2(Cv.x, Cv.y), C23 = f2(Cv.z, Cv.w);
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float dj = j ? dd.y : dd.x;
-        const float2 d2 = bc2(dj), gj = bc2(j ? gg.y : gg.x);
-        dsum[j] += dj;
-        ga[j][0] = mul2(ex2_2(mul2(d2, Ap[j][0])), fma2(gj, C01, ga[j][0]));
-        ga[j][1] = mul2(ex2_2(mul2(d2, Ap[j][1])), fma2(gj, C23, ga[j][1]));
-      }
+      const float2 d2 = bc2(dj);
+      dsum += dj;
+      ga[0] = mul2(ex2_2(mul2(d2, Ap[0])), fma2(gj, f2(Cv.x, Cv.y), ga[0]));
+      ga[1] = mul2(ex2_2(mul2(d2, Ap[1])), fma2(gj, f2(Cv.z, Cv.w), ga[1]));
     }
     __syncthreads();
   }
   if (dvalid) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const size_t row = ((size_t)b * p.sum_stride + sgm) * p.D + dg + j;
-      *reinterpret_cast<float4*>(p.gsum + row * N + n0) = make_float4(ga[j][0].x, ga[j][0].y, ga[j][1].x, ga[j][1].y);
-      if (ng == 0) p.dsum[row] = dsum[j];
-    }
+    const size_t row = ((size_t)b * p.sum_stride + sgm) * p.D + dg;
+    *reinterpret_cast<float4*>(p.gsum + row * N + n0) = make_float4(ga[0].x, ga[0].y, ga[1].x, ga[1].y);
+    if (ng == 0) p.dsum[row] = dsum;
   }
 }
 
@@ -932,7 +933,7 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
   // prefer the largest shared-memory carveout, so that residency (and the occupancy
   // query the segment and grid choices rely on) is limited by the CTAs' own needs
   cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-    skern<<<dim3(pl.ndt, p.B * (p.P - 1)), Geo<N, DT>::NT, smem_s, stream>>>(p, tm[0], tm[2], tm[3], tm[5]);
+    skern<<<dim3(pl.ndt, p.B * (p.P - 1)), GeoS<N, DT>::NT, smem_s, stream>>>(p, tm[0], tm[2], tm[3], tm[5]);
     if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
     if (seg_combine<true>(SegCombine{p.A, p.dsum, p.gsum, p.dh_last, p.gin, p.P, p.D, N, p.P, 1}, p.B, stream) != cudaSuccess)
       return SS_ERR_CUDA;
@@ -995,7 +996,7 @@ int launch_bwd_summary(BwdParams p, const void* delta, const void* Cm, const voi
   p.Ls = p.L;
   p.sum_stride = 1;
   p.sum_first = 0;
-  skern<<<dim3((p.D + SDT - 1) / SDT, p.B), Geo<N, SDT>::NT, smem_s, stream>>>(p, tm[0], tm[1], tm[2], tm[3]);
+  skern<<<dim3((p.D + SDT - 1) / SDT, p.B), GeoS<N, SDT>::NT, smem_s, stream>>>(p, tm[0], tm[1], tm[2], tm[3]);
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
