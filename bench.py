@@ -120,6 +120,7 @@ def alu_co_bounds(wl, ms_fwd, ms_bwd, sms):
         "fp32_fma": {"per_step": fma, "achieved": fma / s, "peak": pk_fma, "unit": "op/s",
                      "frac": round(fma / s / pk_fma, 4), "floor_us": round(fma / pk_fma * 1e6, 1)},
         "peak_from": f"per clock per SM x {sms} SMs x {mhz:.0f} MHz",
+        "measured_pipes": {n: profiled_pipes(n, wl.name) for n in ("scan_fwd", "scan_bwd")},
     }
 
 
@@ -140,6 +141,20 @@ def kernel_source_hash(name):
         with open(os.path.join(ROOT, "mamba_selective_ssm_gb300", "csrc", part), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def profiled_pipes(name, wl_name):
+    """Pipe utilisation of a kernel from a committed ncu summary (profiles/pipes.json), if taken on the current
+    source: issue, FMA-pipe and XU (exponent) fractions of peak."""
+    p = os.path.join(ROOT, "profiles", "pipes.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)[f"{name}:{wl_name}"]
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash(name):
+        return None
+    return {k: rec[k] for k in ("issue_active", "fma_pipe", "xu_pipe", "smem_wavefronts", "warps_per_sm", "how") if k in rec}
 
 
 def profiled_traffic(name, wl_name):
