@@ -112,6 +112,7 @@ PIECE_CASES = [
     ("f32", 16, (48, 80, 17, 64, 1), False, 16),
     ("bf16", 16, (100, 37, 200), True, 8),
     ("bf16", 8, (64, 64, 64, 64), False, 32),
+    ("f32", 4, (30, 2, 70), True, 16),   # a two-step piece, N = 4 (one warp spans 32 channels)
 ]
 
 
