@@ -32,9 +32,10 @@ def all_gather_pieces(t: torch.Tensor, group=None) -> torch.Tensor:
     """Every rank's ``t`` stacked in rank order: [P, *t.shape], on ``t``'s device."""
     world = dist.get_world_size(group)
     if _device_collectives(group):
-        out = torch.empty((world,) + tuple(t.shape), device=t.device, dtype=t.dtype)
-        dist.all_gather_into_tensor(out, t.contiguous(), group=group)
-        return out
+        t = t.contiguous()
+        flat = torch.empty((world * t.numel(),), device=t.device, dtype=t.dtype)  # the ranks' tensors back to back
+        dist.all_gather_into_tensor(flat, t.reshape(-1), group=group)
+        return flat.view((world,) + tuple(t.shape))
     h = t.detach().to("cpu").contiguous()
     parts = [torch.empty_like(h) for _ in range(world)]
     dist.all_gather(parts, h, group=group)
