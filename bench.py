@@ -364,6 +364,62 @@ def time_scan_workload(wl, dev, peak, iters=10, warmup=3):
     return res
 
 
+def time_decode_tokens(wl, dev, stream, p, lib, X, sdt, tdt, T=64, reps=10):
+    """One sequence (B = 1) decoded T tokens at a time through this layer's conv step and SSM step: the per-token
+    time when every call is launched from the host, and when the T tokens' launches are captured once in a CUDA
+    graph and replayed (the library's calls are capturable: no allocation, synchronisation or host read inside).
+    Launch-bound at B = 1: the two kernels move ~1 MB per token."""
+    import torch
+
+    D, N, K = wl.D, wl.N, wl.d_conv
+    g = torch.Generator(device=dev).manual_seed(7)
+    xs = torch.randn((T, 1, D), device=dev, generator=g).to(tdt)
+    dl = (0.001 + 0.099 * torch.rand((T, 1, D), device=dev, generator=g)).to(tdt)
+    zs = torch.randn((T, 1, D), device=dev, generator=g).to(tdt)
+    Bs = torch.randn((T, 1, N), device=dev, generator=g).to(tdt)
+    Cs = torch.randn((T, 1, N), device=dev, generator=g).to(tdt)
+    h = torch.zeros((1, D, N), device=dev, dtype=torch.float32)
+    cs = torch.zeros((1, D, K), device=dev, dtype=torch.float32)
+    u = torch.empty((T, 1, D), device=dev, dtype=tdt)
+    y = torch.empty((T, 1, D), device=dev, dtype=tdt)
+    bias = torch.zeros((D,), device=dev, dtype=torch.float32)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+
+    def tokens(sp_):
+        for t in range(T):
+            if lib.conv1d_causal_step(p(xs[t]), p(cs), p(X["c_w"]), p(bias), p(u[t]), 1, D, K, 1, sdt, sp_) != 0:
+                raise RuntimeError("conv1d_causal_step failed")
+            if lib.ss_scan_step(p(u[t]), p(dl[t]), p(X["A"]), p(Bs[t]), p(Cs[t]), p(X["Dv"]), p(zs[t]), p(h), p(y[t]),
+                                1, D, N, sdt, sp_) != 0:
+                raise RuntimeError("ss_scan_step failed")
+
+    tokens(sp)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        tokens(sp)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us_eager = e0.elapsed_time(e1) * 1e3 / (reps * T)
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        tokens(ctypes.c_void_p(cap.cuda_stream))
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us_graph = e0.elapsed_time(e1) * 1e3 / (reps * T)
+    return {"us_per_token_host_launched": round(us_eager, 2), "us_per_token_cuda_graph": round(us_graph, 2),
+            "tokens": T, "B": 1, "launches_per_token": 2}
+
+
 def profile_run(args):
     """The scan forward + backward (or conv1d fwd/bwd and RMSNorm fwd/bwd) on seeded device tensors of the
     workload's shape (B and L overridable), args.iters times: a fixed, short launch sequence to profile."""
@@ -617,6 +673,7 @@ def main():
             ms = sum(a0.elapsed_time(a1) for a0, a1 in evp) / iters
             gbs = nbytes / (ms * 1e-3) / 1e9
             nxt[n] = {"ms": round(ms, 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        nxt["decode_tokens_b1"] = time_decode_tokens(wl, dev, stream, p, lib, X, sdt, tdt)
 
     # ---- the scan on the other workloads of the method (timed the same way, inputs resident in HBM)
     others = {}
