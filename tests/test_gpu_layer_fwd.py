@@ -50,7 +50,8 @@ def test_conv1d_fwd_full_size_layer(ss):
 
 @pytest.mark.parametrize("R,H,dtype", [(37, 768, "f32"), (64, 2048, "bf16"), (5, 8, "f32"), (1500, 96, "bf16"),
                                        (20000, 32, "f32"), (333, 24, "bf16"), (100, 256, "f32"), (50, 264, "bf16"),
-                                       (3, 12000, "f32"), (2, 32768, "bf16"), (8192, 2048, "bf16")])
+                                       (3, 12000, "f32"), (2, 32768, "bf16"), (8192, 2048, "bf16"), (41, 1536, "f32"),
+                                       (700, 2040, "bf16"), (9, 4096, "bf16")])
 def test_rmsnorm_fwd_parity(ss, R, H, dtype):
     wl = CONFIGS["tiny"].with_(dtype=dtype)
     r = make_rmsnorm_inputs(wl, seed=R + 1, rows=R, dim=H)
