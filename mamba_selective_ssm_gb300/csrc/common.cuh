@@ -81,7 +81,13 @@ __device__ __forceinline__ float2 ex2_2(float2 u) { return make_float2(ex2(u.x),
 
 // ---------------------------------------------------------------- dtypes
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+// the low bf16 of a pair: the 16-bit shift written as an integer multiply, which issues on the FMA pipe rather
+// than the ALU pipe the other half's mask and the pair packing already load (RMSNorm forward 15.3 -> 15.0 us)
+__device__ __forceinline__ float bf16_lo(uint32_t w) {
+  uint32_t r;
+  asm("mul.lo.u32 %0, %1, 65536;" : "=r"(r) : "r"(w));
+  return __uint_as_float(r);
+}
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 template <typename T>
