@@ -17,8 +17,8 @@
 // instead: a thread walks the input steps t of its tile and K-1 beyond, turns
 // each incoming dout[t] into g[t] = dout[t] * silu'(pre[t]) with
 // pre[t] = bias + sum_k w[k] x[t-(K-1)+k] recomputed from the x window behind
-// t, and completes dx[t-(K-1)] from the last K values of g; the loads of four
-// steps are issued together.  The four-channel arithmetic runs as packed
+// t, and completes dx[t-(K-1)] from the last K values of g; the loads of eight
+// steps are issued together, at three CTAs per SM.  The four-channel arithmetic runs as packed
 // f32x2 operations (two per step where scalar code takes four).
 #include "common.cuh"
 
@@ -28,6 +28,7 @@ using namespace ssk;
 
 constexpr int kCTile = 16;     // time steps per tile (short tiles: the (batch row, tile) items spread evenly over the CTAs)
 constexpr int kCTileSilu = 24;  // the SiLU-fused form recomputes K-1 steps of g per tile (16: 84 us, 24: 81, 32: 82)
+constexpr int kCtasSilu = 3;    // SiLU-fused form: CTAs per SM (~170 registers for its eight loads in flight)
 constexpr int kCThreads = 128;  // threads per CTA: 512 channels
 
 template <typename T>
@@ -80,7 +81,7 @@ __device__ __forceinline__ float4 f4z() { return make_float4(0.f, 0.f, 0.f, 0.f)
 
 
 template <int K, typename T, bool SILU>
-__global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __restrict__ dout, const T* __restrict__ x,
+__global__ void __launch_bounds__(kCThreads, SILU ? kCtasSilu : 4) conv_bwd_kernel(const float* __restrict__ dout, const T* __restrict__ x,
                                                              const float* __restrict__ w, const float* __restrict__ bias,
                                                              float* __restrict__ dx, float* __restrict__ ws, int B, int L,
                                                              int D) {
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(kCThreads, 4) conv_bwd_kernel(const float* __r
   if (valid && SILU) {
     // walk the input steps t = t0 .. t1+K-2: g[t] is formed once from the x window behind t, enters dw / db
     // when t < t1, and completes dx[t-(K-1)] when that is in the tile; loads issued U steps at a time
-    constexpr int U = 4;  // loads issued together (8 spills at 128 registers; 2 slower)
+    constexpr int U = 8;  // loads issued together, at three CTAs per SM (four CTAs with 4 loads: 80.4 us, 78.5 here)
     using R = RawX4<T>;
     for (int bt = blockIdx.y * ipc + sub; bt < B * ntt; bt += gridDim.y * ipc) {
       const int b = bt / ntt, t0 = (bt % ntt) * TILE;
@@ -252,10 +253,19 @@ int conv_validate(int B, int L, int D, int K, int x_dtype) {
 template <int K, typename T, bool SILU>
 int conv_launch(const float* dout, const void* x, const float* w, const float* bias, float* dx, float* dw, float* db,
                 int B, int L, int D, float* ws, const ConvPlan& pl, cudaStream_t s) {
+  // one wave: the SiLU-fused form holds three CTAs per SM, so it runs fewer CTA rows (and partial rows)
+  int gy = pl.gy, rows = pl.rows;
+  if (SILU) {
+    const int cap = (kCtasSilu * device_sm_count()) / pl.gx > 0 ? (kCtasSilu * device_sm_count()) / pl.gx : 1;
+    if (gy > cap) {
+      rows = rows / gy * cap;
+      gy = cap;
+    }
+  }
   conv_bwd_kernel<K, T, SILU>
-      <<<dim3(pl.gx, pl.gy), kCThreads, 0, s>>>(dout, static_cast<const T*>(x), w, bias, dx, ws, B, L, D);
+      <<<dim3(pl.gx, gy), kCThreads, 0, s>>>(dout, static_cast<const T*>(x), w, bias, dx, ws, B, L, D);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
-  return colsum(ws, (long long)D * (K + 1), pl.rows, ConvStore{dw, db, D, K}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  return colsum(ws, (long long)D * (K + 1), rows, ConvStore{dw, db, D, K}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 }  // namespace
