@@ -923,7 +923,10 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
     p.Ls = sp.Ls;
     p.sum_stride = sp.P;
   }
-  int rows = pl.gy;
+  // CTA rows walk their batch rows: one wave of equal CTAs when the rows do not fit at once
+  // (at most pl.gy, the dA/dD partial rows the workspace holds)
+  int rows = balanced_rows(p.B, pl.ndt, (long long)per_sm * device_sm_count());
+  if (rows > pl.gy) rows = pl.gy;
   if (p.P > 1) {
     rows = p.B * p.P;
     const size_t smem_s = sizeof(BwdSumSmem<T, N, kSumStages, DT>);

@@ -57,6 +57,17 @@ struct SegPlan {
   int P, Ls;
 };
 
+// CTA rows of a grid whose CTAs walk batch rows y, y + gy, ...: all B rows at
+// once when the B x tiles CTAs fit the `resident` slots, else the fewest rows
+// of CTAs that fit and give every CTA the same number of batch rows up to one
+// (one wave of equal CTAs instead of a full wave and a partial one).
+inline int balanced_rows(int B, int tiles, long long resident) {
+  const long long fit = tiles > 0 ? resident / tiles : 0;
+  if (fit < 1 || fit >= B) return fit < 1 ? 1 : B;
+  const long long per = (B + fit - 1) / fit;  // batch rows per CTA
+  return (int)((B + per - 1) / per);
+}
+
 // Segments of equal length (a multiple of unit) covering L with about p_want pieces.
 inline SegPlan seg_plan(int p_want, int L, int unit) {
   if (p_want <= 1) return SegPlan{1, L};

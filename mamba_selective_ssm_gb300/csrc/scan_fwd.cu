@@ -344,8 +344,10 @@ int launch_fwd(FwdParams p, const void* x, const void* delta, const void* Bm, co
       return SS_ERR_CUDA;
     kern<<<dim3(ndt, p.B * p.P), 32, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
   } else {
-    const int cap = 8192 / ndt > 0 ? 8192 / ndt : 1;  // at most ~8192 CTAs; each loops over its batch rows
-    const int gy = p.B < cap ? p.B : cap;
+    // every CTA loops over its batch rows: one wave of equal CTAs when the rows do not fit at once
+    const int per_sm = resident_ctas(kern, 32, smem);
+    if (per_sm < 1) return SS_ERR_CUDA;
+    const int gy = balanced_rows(p.B, ndt, (long long)per_sm * device_sm_count());
     kern<<<dim3(ndt, gy), 32, smem, stream>>>(p, tm[0], tm[1], tm[2], tm[3], tm[4]);
   }
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
