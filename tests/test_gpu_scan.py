@@ -96,8 +96,9 @@ def test_scan_h0_dh_last_and_accumulation(ss, dtype, chunk):
 
 
 def test_scan_rows_beyond_the_first_batch_row_use_their_own_state(ss):
-    """Each CTA loops over several batch rows: the short many-batch shape with B above the grid cap."""
-    B, L, D, N, chunk = 1100, 16, 8, 16, 16
+    """Each CTA walks several batch rows: the short many-batch shape with more (row, channel tile) pairs than
+    resident CTAs in both directions, B odd so that some CTAs get one row fewer than others."""
+    B, L, D, N, chunk = 3001, 16, 8, 16, 16
     wl = CONFIGS["short"].with_(B=B, L=L, D=D, N=N, chunk=chunk)
     inp = make_scan_inputs(wl, seed=11)
     d = scan_inputs_on_device(inp, "f32")
