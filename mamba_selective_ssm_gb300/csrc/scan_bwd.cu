@@ -2,7 +2,8 @@
 // time through the diagonal SSM state, with the states rebuilt from the
 // forward's chunk checkpoints instead of a stored [B, L, D, N] history.
 //
-// One CTA = 32 channels (64 when N = 4) of one batch row at a time.  Chunks are visited from
+// One CTA = 32 channels (64 when N = 4, or when a chunk's parked states take
+// 128 TMEM columns or more) of one batch row at a time.  Chunks are visited from
 // last to first; each chunk (a multiple of 16 steps) is walked twice:
 //   pass A (tiles in order):   from the chunk's checkpoint, advance
 //       h_t = a_t h_{t-1} + delta_t B_t x_t and park the state entering every

@@ -39,9 +39,10 @@ struct Geo {
 // When a layer has too few (batch, channel-tile) pairs to fill the GPU, the
 // sequence is cut into P segments of Ls steps (a multiple of `unit`).  A
 // summary kernel computes each segment's contribution from a zero carry and
-// its total step size sum(delta); a main-kernel CTA then composes its own
-// carry from the summaries of the segments before (forward) or after
-// (backward) it:  carry <- exp2(A log2e * sum(delta)) * carry + contribution.
+// its total step size sum(delta); seg_combine_kernel below composes the maps
+// carry <- exp2(A log2e * sum(delta)) * carry + contribution of the segments
+// before (forward) or after (backward) each one, and the main kernel runs
+// every segment from its carry.
 
 // Upper bound on P used to size the summary workspace: aims at about `target`
 // CTAs in all (16 per SM of 152 by default).
