@@ -230,3 +230,62 @@ def test_two_gloo_ranks_on_one_gpu_match_the_whole_sequence(ss):
         for k in ("dA", "dD", "d_dt_bias"):
             assert_close(got[r][k], g[k], tol, f"{k} rank {r}")
     assert_close(got[0]["dh0"], g["dh0"], tol, "dh0")
+
+
+def _nccl_one_rank_worker(port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), NCCL_NVLS_ENABLE="0")
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    from mamba_selective_ssm_gb300 import ops, sharded
+    from tests.gpu_util import dev as dev_, host as host_
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda", 0))
+    try:
+        rng = np.random.default_rng(5)
+        t = dev_(rng.standard_normal((2, 24, 16)))
+        u = dev_(rng.standard_normal((24,)))
+        g = sharded.all_gather_pieces(t)
+        u0 = u.clone()
+        sharded.all_reduce_sum_(u)
+        c = RANK_CASE
+        inp = make_scan_inputs(_wl(c["B"], sum(c["pieces"]), c["D"], c["N"], c["dtype"]), seed=78)
+        p = {k: dev_(inp[k], c["dtype"]) for k in ("x", "delta_raw", "z", "Bm", "Cm", "dy")}
+        A, Dv, bias = dev_(inp["A"]), dev_(inp["Dv"]), dev_(inp["dt_bias"])
+        kw = dict(dt_bias=bias, delta_softplus=True)
+        a = (p["x"], p["delta_raw"], A, p["Bm"], p["Cm"], Dv, p["z"])
+        y, ck, hl, _ = sharded.ss_scan_fwd_sharded(*a, chunk=c["chunk"], **kw)
+        gs = sharded.ss_scan_bwd_sharded(*a, ck, p["dy"], chunk=c["chunk"], **kw)
+        # the exchange the ranks of a larger group run, through the device collectives: one piece composes to h0
+        h0 = dev_(rng.standard_normal((c["B"], c["D"], c["N"])))
+        h_end, dsum = ops.ss_scan_fwd_summary(p["x"], p["delta_raw"], A, p["Bm"], **kw)
+        carry = ops.ss_scan_carries(A, sharded.all_gather_pieces(dsum), sharded.all_gather_pieces(h_end), init=h0)
+        y1, ck1, hl1 = ops.ss_scan_fwd(*a, chunk=c["chunk"], **kw)
+        g1 = ops.ss_scan_bwd(*a, ck1, p["dy"], chunk=c["chunk"], **kw)
+        torch.cuda.synchronize()
+        q.put({"backend": dist.get_backend(), "gather_shape": tuple(g.shape), "gather_same": bool(torch.equal(g[0], t)),
+               "carry_shape": tuple(carry.shape), "carry_err": float((carry[0] - h0).abs().max() / h0.abs().max()),
+               "reduce_same": bool(torch.equal(u, u0)), "y_same": bool(torch.equal(y, y1)),
+               "h_last_same": bool(torch.equal(hl, hl1)),
+               "grads_same": {k: bool(torch.equal(v, g1[k])) for k, v in gs.items() if v is not None and k in g1}})
+    finally:
+        dist.destroy_process_group()
+
+
+def test_one_nccl_rank_runs_the_device_exchange(ss):
+    """The NCCL branch of the exchange (all-gather into one device tensor, device all-reduce) with a single rank:
+    no peer to wait on, so it runs on this one GPU; the whole sequence as one piece equals the unsharded calls."""
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    proc = ctx.Process(target=_nccl_one_rank_worker, args=(_free_port(), q))
+    proc.start()
+    got = q.get(timeout=600)
+    proc.join(timeout=120)
+    assert proc.exitcode == 0
+    assert got["backend"] == "nccl"
+    assert got["gather_shape"] == (1, 2, 24, 16) and got["gather_same"]
+    assert got["reduce_same"]
+    assert got["carry_shape"] == (1, RANK_CASE["B"], RANK_CASE["D"], RANK_CASE["N"]) and got["carry_err"] <= 1e-6
+    assert got["y_same"] and got["h_last_same"]
+    assert got["grads_same"] and all(got["grads_same"].values()), got["grads_same"]
