@@ -134,6 +134,15 @@ struct GeoS {
   static_assert(W >= 1 && DT % CPW == 0, "a CTA holds whole warps");
 };
 
+// Channels per summary CTA: one warp's worth.  A one-warp CTA's tile barrier
+// costs nothing, where eight-warp CTAs stalled on it (long-context backward
+// 1006 -> 964 us, with four staging slots instead of six so that the narrower
+// CTAs, which share less of the B_t/C_t staging, still all fit at once).
+template <int N>
+constexpr int sum_dt() {
+  return GeoS<N, 32 / (N / 4)>::CPW;
+}
+
 // Segment summaries: for each segment the adjoint it carries out of its first
 // step when the carry entering its last step is zero, and its sum of delta.
 // CTA = (channel tile, (batch row, segment)); tiles walked last to first.
@@ -860,8 +869,8 @@ template <typename T>
 struct Stages {
   static constexpr int value = 1;
 };
-// the summary kernel's tiles take a few hundred cycles each: six in flight
-constexpr int kSumStages = 6;
+// the summary kernel's tiles take a few hundred cycles each: four in flight per one-warp CTA
+constexpr int kSumStages = 4;
 
 template <int N, typename T, int NSTG, int DT, bool FUSE>
 int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, const void* Cm, const void* z, const void* dy,
@@ -930,14 +939,22 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
   if (rows > pl.gy) rows = pl.gy;
   if (p.P > 1) {
     rows = p.B * p.P;
-    const size_t smem_s = sizeof(BwdSumSmem<T, N, kSumStages, DT>);
-    auto skern = scan_bwd_summary_kernel<N, T, kSumStages, DT, FUSE>;
+    constexpr int SDT = sum_dt<N>();
+    const uint32_t sbox[3] = {SDT, kTT, 1};
+    CUtensorMap ts[3];  // delta, z, dy in the summary's narrower boxes
+    if (!ssh::encode_tiled(&ts[0], ActT<T>::kTma, 3, delta, adims, astr, sbox) ||
+        !ssh::encode_tiled(&ts[1], ActT<T>::kTma, 3, z, adims, astr, sbox) ||
+        !ssh::encode_tiled(&ts[2], ActT<T>::kTma, 3, dy, adims, astr, sbox))
+      return SS_ERR_CUDA;
+    const size_t smem_s = sizeof(BwdSumSmem<T, N, kSumStages, SDT>);
+    auto skern = scan_bwd_summary_kernel<N, T, kSumStages, SDT, FUSE>;
     if (cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s) != cudaSuccess)
       return SS_ERR_CUDA;
   // prefer the largest shared-memory carveout, so that residency (and the occupancy
   // query the segment and grid choices rely on) is limited by the CTAs' own needs
   cudaFuncSetAttribute(skern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-    skern<<<dim3(pl.ndt, p.B * (p.P - 1)), GeoS<N, DT>::NT, smem_s, stream>>>(p, tm[0], tm[2], tm[3], tm[5]);
+    skern<<<dim3((p.D + SDT - 1) / SDT, p.B * (p.P - 1)), GeoS<N, SDT>::NT, smem_s, stream>>>(p, ts[0], ts[1], ts[2],
+                                                                                           tm[5]);
     if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
     if (seg_combine<true>(SegCombine{p.A, p.dsum, p.gsum, p.dh_last, p.gin, p.P, p.D, N, p.P, 1}, p.B, stream) != cudaSuccess)
       return SS_ERR_CUDA;
@@ -978,7 +995,7 @@ int validate_bwd(int B, int L, int D, int N, int chunk, int dtype) {
 template <int N, typename T, bool FUSE>
 int launch_bwd_summary(BwdParams p, const void* delta, const void* Cm, const void* z, const void* dy, cudaStream_t stream) {
   constexpr int e = ActT<T>::kBytes;
-  constexpr int SDT = bwd_dt<N>();
+  constexpr int SDT = sum_dt<N>();
   const uint64_t adims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
   const uint64_t astr[2] = {(uint64_t)p.D * e, (uint64_t)p.L * p.D * e};
   const uint32_t sbox[3] = {SDT, kTT, 1};
