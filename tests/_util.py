@@ -28,7 +28,8 @@ def max_rel_err(got, ref) -> float:
     return diff / scale
 
 
-# Diagnostic beside the parity metric (the survey's reading of the pages' undefined "max relative error"):
+# Diagnostic beside the parity metric (a second reading of the "max relative error" that the rustytorch
+# backward_cuda commit states without defining it):
 # the largest elementwise relative error |g_i - r_i| / |r_i| over the elements that carry the tensor,
 # |r_i| >= 1e-2 max|r|.  It sees a wrong element whose reference is small, which the infinity-norm metric
 # can hide.  Bound: ELEM_TOL; observed values are recorded for the session report.
