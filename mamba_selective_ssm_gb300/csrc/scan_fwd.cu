@@ -6,13 +6,13 @@
 // (N/4)).  Lane (ng, c) owns channel c and states 4ng .. 4ng+3: four (d, n)
 // recurrences in registers, f32x2-packed, with one ex2 per (t, d, n) (A
 // pre-scaled by log2 e).  The sequence is walked once, in order, in 16-step
-// tiles that TMA stages into a 4-deep ring.  The recurrence reads delta and x
-// straight from the staging slot; B_t and C_t, shared by every lane of a state
-// quad, are widened to fp32 once per tile so that each step loads them with
-// one 128-bit broadcast read.  C_t . h_t is summed over the N/4 lanes of a
-// channel by a shuffle reduce-scatter over four steps (two when N = 8), after
-// which every lane holds the complete sum of one (t, d) and forms
-// y = (s + D x) * silu(z) itself.  A warp needs no block barrier: copies are
+// tiles that TMA stages into a ring (2 deep for bf16, 3 for fp32).  The
+// recurrence reads delta and x straight from the staging slot; B_t and C_t,
+// shared by every lane of a state quad, are widened to fp32 once per tile so
+// that each step loads them with one 128-bit broadcast read.  C_t . h_t is
+// summed over the N/4 lanes of a channel by a shuffle reduce-scatter over four
+// steps (two when N = 8), after which every lane holds the complete sum of one
+// (t, d) and forms y = (s + D x) * silu(z) itself.  A warp needs no block barrier: copies are
 // observed on mbarriers and slot reuse is ordered by warp syncs, so the ~13
 // warps an SM holds on a Mamba-sized layer never wait on one another.
 // The state entering step c*chunk is stored as checkpoint c ([B, chunks, D, N])
@@ -31,7 +31,15 @@ using namespace ssk;
 
 __device__ unsigned g_fwd_err;
 
-constexpr int kNST = 4;  // TMA pipeline depth (tiles in flight)
+// TMA pipeline depth (tiles in flight per one-warp CTA).  Fewer slots leave
+// room for more resident CTAs, which the segment and grid choices turn into
+// parallelism: two for bf16, three for fp32 (against four: long-context
+// forward 361 -> 332 us, short many-batch 67 -> 60 / 64 us, mamba130m
+// 212 -> 205 us with three, the 1.4B layer unchanged).
+template <typename T>
+constexpr int fwd_stages() {
+  return sizeof(T) == 2 ? 2 : 3;
+}
 
 struct FwdParams {
   const float* A;
@@ -62,6 +70,7 @@ struct GeoW {
 template <typename T, int N>
 struct FwdSmem {
   static constexpr int DT = GeoW<N>::DT;
+  static constexpr int kNST = fwd_stages<T>();
   alignas(128) T dlt[kNST][kTT * DT];
   alignas(128) T x[kNST][kTT * DT];
   alignas(128) T z[kNST][kTT * DT];
@@ -86,6 +95,7 @@ __global__ void __launch_bounds__(32) scan_fwd_kernel(const FwdParams p, const _
   using G = GeoW<N>;
   using AT = ActT<T>;
   constexpr int NG = G::NG, CG = G::CG, DT = G::DT;
+  constexpr int kNST = FwdSmem<T, N>::kNST;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   FwdSmem<T, N>& S = *reinterpret_cast<FwdSmem<T, N>*>(smem_raw);
 
