@@ -67,7 +67,7 @@ CONFIGS = {
     "mamba1p4b": Workload("mamba1p4b", 4, 2048, 4096, 16, 4, 2048, "bf16", 1e-3, 1e-1, 8,
                           "Mamba-1.4B-shaped layer: B=4, L=2048, d_model=2048, d_inner=4096, N=16, "
                           "bf16 x/delta/B/C/z/dy, fp32 state and grads"),
-    "short": Workload("short", 4096, 32, 64, 16, 4, 32, "f32", 1e-3, 1e-1, 32,
+    "short": Workload("short", 4096, 32, 64, 16, 4, 32, "f32", 1e-3, 1e-1, 8,
                       "short-sequence many-batch scan: B=4096, L=32, d_inner=64, N=16, fp32"),
     "long": Workload("long", 1, 16384, 2048, 16, 4, 1024, "bf16", 1e-4, 1e-2, 256,
                      "long-context scan: B=1, L=16384, d_inner=2048, N=16, bf16, long-memory delta, "
