@@ -42,6 +42,11 @@ constexpr int bwd_dt() {
   return Geo<N, 64>::WC > 32 ? 64 : 32;
 }
 
+// Window groups of a backward CTA: two when a 64-channel CTA has four warps (N = 16), else one.
+__host__ __device__ constexpr int bwd_groups(int N, int DT) {
+  return (DT == 64 && N == 16) ? 2 : 1;
+}
+
 template <typename T, int N, int NSTG, int DT>
 struct BwdSmem {
   static constexpr int W = Geo<N, DT>::W, CG = Geo<N, DT>::CG;
@@ -93,7 +98,7 @@ struct BwdParams {
   float* ddelta;
   float* dz;
   float* dh0;
-  float* ws_dBC;  // [channel tiles][B][L][2N]
+  float* ws_dBC;  // [channel tiles x window groups][B][L][2N]
   float* ws_dAD;  // [CTA rows][D*N + 2D]: dA, dD and d dt_bias partials of each CTA row
   int B, L, D, chunk, nchunks;
   uint32_t tcols;
@@ -284,6 +289,17 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
   const int nitems = nb * per_b;
   constexpr uint32_t kActBytes = kTT * DT * AT::kBytes;
   constexpr uint32_t kBCBytes = kTT * N * AT::kBytes;
+  // A four-warp CTA (64 channels, so that the TMEM of a long chunk is used on
+  // all 128 lanes) closes its windows as two 32-channel groups of two warps,
+  // each with its own barrier and its own dB/dC partial: a window then waits
+  // for one other warp instead of three.  Tiles (staging, widening) stay CTA-wide.
+  constexpr int GRP = bwd_groups(N, DT);
+  constexpr int GT = G::NT / GRP, GW = G::W / GRP, GDT = DT / GRP;
+  const int grp = warp / GW, gtid = tid - grp * GT;
+  auto group_sync = [&]() {
+    if constexpr (GRP == 1) __syncthreads();
+    else asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(GT) : "memory");
+  };
 
   float2 Ap[2][2];
 #pragma unroll
@@ -646,28 +662,29 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
         *reinterpret_cast<float4*>(&S.sab[i][ng][2 * dl]) = make_float4(sA[0], sB[0], sA[1], sB[1]);
         *reinterpret_cast<float4*>(&S.dbc[warp][i][0][cg * N + n0]) = make_float4(db0.x, db0.y, db1.x, db1.y);
       }
-      __syncthreads();
+      group_sync();
 
-      // window epilogue.  dB_t, dC_t of this tile of 64 channels: lanes and warps in fixed order
-      for (int e = tid; e < kS * N / 2; e += G::NT) {  // (row, dB | dC, group of 4 states)
+      // window epilogue.  dB_t, dC_t of this group's channels: lanes and warps in fixed order
+      for (int e = gtid; e < kS * N / 2; e += GT) {  // (row, dB | dC, group of 4 states)
         const int i = e / (N / 2), qq = (e % (N / 2)) / (N / 4), n4 = (e % (N / 4)) * 4;
         const int t = t0 + sub * kS + i;
         float2 a01 = f2(0.f, 0.f), a23 = f2(0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < G::W; ++w)
+        for (int w = 0; w < GW; ++w)
 #pragma unroll
           for (int c = 0; c < G::CG; ++c) {
-            const float4 v = *reinterpret_cast<const float4*>(&S.dbc[w][i][qq][c * N + n4]);
+            const float4 v = *reinterpret_cast<const float4*>(&S.dbc[grp * GW + w][i][qq][c * N + n4]);
             a01 = add2(a01, f2(v.x, v.y));
             a23 = add2(a23, f2(v.z, v.w));
           }
         if (t < L)
-          *reinterpret_cast<float4*>(&p.ws_dBC[(((size_t)blockIdx.x * p.B + b) * L + t) * (2 * N) + qq * N + n4]) =
+          *reinterpret_cast<float4*>(
+              &p.ws_dBC[(((size_t)(blockIdx.x * GRP + grp) * p.B + b) * L + t) * (2 * N) + qq * N + n4]) =
               make_float4(a01.x, a01.y, a23.x, a23.y);
       }
-      // per-(t, d) gradients, four channels per thread
-      for (int gi = tid; gi < kS * DT / 4; gi += G::NT) {
-        const int i = gi / (DT / 4), c4 = (gi % (DT / 4)) * 4;
+      // per-(t, d) gradients of this group's channels, four channels per thread
+      for (int gi = gtid; gi < kS * GDT / 4; gi += GT) {
+        const int i = gi / (GDT / 4), c4 = grp * GDT + (gi % (GDT / 4)) * 4;
         const int rr = sub * kS + i;
         const int t = t0 + rr, d = d0 + c4;
         if (t < L && d < p.D) {
@@ -723,7 +740,7 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
           *reinterpret_cast<float4*>(p.dz + off) = make_float4(o2[0], o2[1], o2[2], o2[3]);
         }
       }
-      __syncthreads();
+      group_sync();
     }
 
     if (t0 == 0 && p.dh0 != nullptr && dvalid) {  // last item of batch row b: ga = a_0 G_0
@@ -755,16 +772,16 @@ __global__ void __launch_bounds__(Geo<N, DT>::NT) scan_bwd_kernel(const BwdParam
       *reinterpret_cast<float4*>(row + (size_t)(dg + j) * N + n0) =
           make_float4(dA2[j][0].x, dA2[j][0].y, dA2[j][1].x, dA2[j][1].y);
   }
-  // dD, d dt_bias: threads with equal tid % (DT/4) hold the same four channels
+  // dD, d dt_bias: the threads of a group with equal gtid % (GDT/4) hold the same four channels
   float* red = &S.sab[0][0][0];  // free after the last window
   *reinterpret_cast<float4*>(&red[tid * 4]) = make_float4(dDacc[0], dDacc[1], dDacc[2], dDacc[3]);
   *reinterpret_cast<float4*>(&red[(G::NT + tid) * 4]) = make_float4(dTacc[0], dTacc[1], dTacc[2], dTacc[3]);
   __syncthreads();
   for (int c = tid; c < DT; c += G::NT) {
     if (d0 + c < p.D) {
-      const int grp = c / 4, e = c % 4;
+      const int g0 = c / GDT, q4 = (c % GDT) / 4, e = c % 4;
       float accD = 0.f, accT = 0.f;
-      for (int m = grp; m < G::NT; m += DT / 4) {
+      for (int m = g0 * GT + q4; m < (g0 + 1) * GT; m += GDT / 4) {
         accD += red[m * 4 + e];
         accT += red[(G::NT + m) * 4 + e];
       }
@@ -841,19 +858,21 @@ inline int bwd_seg_unit(int chunk) { return chunk > kTT ? chunk : kTT; }
 
 struct BwdPlan {
   int ndt, gy, pmax;
+  int ngr;  // dB/dC partial tiles: one per channel tile, or per window group of a tile
   size_t off_dAD, off_gsum, off_dsum, off_gin, total;
 };
 
 inline BwdPlan make_plan(int B, int L, int D, int N, int chunk) {
   BwdPlan pl;
   pl.ndt = (D + bwd_channels(N, chunk) - 1) / bwd_channels(N, chunk);
+  pl.ngr = pl.ndt * bwd_groups(N, bwd_channels(N, chunk));
   const int cap = 1024 / pl.ndt > 0 ? 1024 / pl.ndt : 1;
   pl.gy = B < cap ? B : cap;
   const long long ctas = (long long)pl.ndt * B;
   pl.pmax = ctas >= 608 ? 1 : seg_pmax(ctas, L, bwd_seg_unit(chunk));
   const int rows = pl.pmax > 1 && B * pl.pmax > pl.gy ? B * pl.pmax : pl.gy;
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
-  pl.off_dAD = up((size_t)pl.ndt * B * L * 2 * N * sizeof(float));
+  pl.off_dAD = up((size_t)pl.ngr * B * L * 2 * N * sizeof(float));
   pl.off_gsum = up(pl.off_dAD + (size_t)rows * D * (N + 2) * sizeof(float));
   const size_t st = pl.pmax > 1 ? (size_t)B * pl.pmax * D * N * sizeof(float) : 0;
   pl.off_dsum = up(pl.off_gsum + st);
@@ -967,7 +986,7 @@ int launch_bwd_f(BwdParams p, const void* x, const void* delta, const void* Bm, 
   const long long nA = (long long)p.D * N, nAD = nA + 2ll * p.D;
   const long long blk_ad = (nAD + 31) / 32;
   const cudaError_t err = launch_dependent(ss_bwd_reduce_kernel<N>, dim3((unsigned)(blk_bc + blk_ad)), dim3(256), 0, stream,
-                                         (const float*)p.ws_dBC, dB, dC, nBC, pl.ndt, (int)blk_bc, (const float*)p.ws_dAD,
+                                         (const float*)p.ws_dBC, dB, dC, nBC, pl.ngr, (int)blk_bc, (const float*)p.ws_dAD,
                                          nAD, rows, DADStore{dA, dD, p.d_dt_bias, nA, p.D});
   return err == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
