@@ -292,6 +292,7 @@ struct AddTo {
 
 struct RmsPlan {
   int vpt, threads, grid;
+  int cgrid;  // partial rows the column-split kernel may use (rows of 257 .. 2048 columns)
   size_t bytes;
 };
 
@@ -301,7 +302,11 @@ inline RmsPlan rms_plan(int rows, int dim) {
   p.vpt = groups <= 1024 ? 1 : groups <= 2048 ? 2 : 4;
   p.threads = ((groups + p.vpt - 1) / p.vpt + 31) / 32 * 32;
   p.grid = rows < 608 ? rows : 608;  // 4 waves of 152 SMs; each CTA walks rows/608 rows
-  p.bytes = (size_t)p.grid * dim * sizeof(float);
+  // narrow rows make small column-split CTAs (dim/64 warps): allow enough of them for ~32 warps per SM
+  const int cw = (dim / 8 + 31) / 32;
+  const int cap = dim > 256 && dim <= 2048 ? 152 * (32 / cw > 4 ? 32 / cw : 4) : 608;
+  p.cgrid = rows < cap ? rows : cap;
+  p.bytes = (size_t)(p.cgrid > p.grid ? p.cgrid : p.grid) * dim * sizeof(float);
   return p;
 }
 
@@ -479,7 +484,7 @@ int rms_cols_launch(const void* dy, const void* x, const float* scale, const flo
   long long grid = (long long)per_sm * device_sm_count();
   const long long need = ((long long)rows + R - 1) / R;
   if (grid > need) grid = need;
-  if (grid > pl.grid) grid = pl.grid;  // the workspace holds pl.grid partial rows
+  if (grid > pl.cgrid) grid = pl.cgrid;  // the workspace holds pl.cgrid partial rows
   if (grid < 1) grid = 1;
   kern<<<(int)grid, threads, 0, s>>>(static_cast<const T*>(dy), static_cast<const T*>(x), scale, rms, dx, ws, rows, dim);
   if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
