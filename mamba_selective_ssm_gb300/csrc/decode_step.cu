@@ -19,6 +19,11 @@ using namespace ssk;
 
 constexpr int kStepThreads = 256;
 
+// CTA (blockIdx.x = sequence b, blockIdx.y = a run of kStepU * kStepThreads
+// (channel, state quad) slots of that sequence): each thread advances kStepU
+// state vectors, with all their loads issued before the arithmetic.
+constexpr int kStepU = 2;
+
 template <int N, typename T>
 __global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const T* __restrict__ x, const T* __restrict__ delta,
                                                                const float* __restrict__ A, const T* __restrict__ Bm,
@@ -27,69 +32,105 @@ __global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const T* __restri
                                                                T* __restrict__ y, int B, int D) {
   using AT = ActT<T>;
   constexpr int NG = N / 4;  // lanes per channel
-  const long long gid = (long long)blockIdx.x * kStepThreads + threadIdx.x;
-  const long long q = gid / NG;  // channel index over B*D
-  const int ng = (int)(gid % NG);
-  const bool ok = q < (long long)B * D;
-  const int b = ok ? (int)(q / D) : 0, d = ok ? (int)(q % D) : 0;
-  float part = 0.f, xd = 0.f;
-  if (ok) {
-    const float dt = AT::ld(delta + q);
-    xd = AT::ld(x + q);
-    const float4 a4 = *reinterpret_cast<const float4*>(A + (size_t)d * N + ng * 4);
-    float4 hv = *reinterpret_cast<const float4*>(h + q * N + ng * 4);
-    const T* bb = Bm + (size_t)b * N + ng * 4;
-    const T* cc = Cm + (size_t)b * N + ng * 4;
-    const float dx = dt * xd;
-    hv.x = fmaf(ex2(dt * (a4.x * kLog2e)), hv.x, dx * AT::ld(bb + 0));
-    hv.y = fmaf(ex2(dt * (a4.y * kLog2e)), hv.y, dx * AT::ld(bb + 1));
-    hv.z = fmaf(ex2(dt * (a4.z * kLog2e)), hv.z, dx * AT::ld(bb + 2));
-    hv.w = fmaf(ex2(dt * (a4.w * kLog2e)), hv.w, dx * AT::ld(bb + 3));
-    *reinterpret_cast<float4*>(h + q * N + ng * 4) = hv;
-    part = fmaf(AT::ld(cc + 0), hv.x, fmaf(AT::ld(cc + 1), hv.y, fmaf(AT::ld(cc + 2), hv.z, AT::ld(cc + 3) * hv.w)));
+  const int b = (int)blockIdx.x;
+  const T* bb = Bm + (size_t)b * N;
+  const T* cc = Cm + (size_t)b * N;
+  float4 hv[kStepU], a4[kStepU];
+  float dt[kStepU], xd[kStepU];
+  bool ok[kStepU];
+  int d[kStepU], ng[kStepU];
+#pragma unroll
+  for (int u = 0; u < kStepU; ++u) {
+    const int slot = ((int)blockIdx.y * kStepU + u) * kStepThreads + (int)threadIdx.x;  // d * NG + ng
+    d[u] = slot / NG;
+    ng[u] = slot % NG;
+    ok[u] = d[u] < D;
+    const size_t q = (size_t)b * D + (ok[u] ? d[u] : 0);
+    dt[u] = ok[u] ? AT::ld(delta + q) : 0.f;
+    xd[u] = ok[u] ? AT::ld(x + q) : 0.f;
+    a4[u] = ok[u] ? *reinterpret_cast<const float4*>(A + (size_t)d[u] * N + ng[u] * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    hv[u] = ok[u] ? *reinterpret_cast<const float4*>(h + q * N + ng[u] * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
-  for (int o = 1; o < NG; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if (ok && ng == 0) {
-    const float zz = AT::ld(z + q);
-    const float s = fmaf(Dv[d], xd, part);
-    const float o = s * zz * sigmoid(zz);
-    if constexpr (sizeof(T) == 4) y[q] = o;
-    else y[q] = __float2bfloat16_rn(o);
+  for (int u = 0; u < kStepU; ++u) {
+    const size_t q = (size_t)b * D + (ok[u] ? d[u] : 0);
+    const T* bq = bb + ng[u] * 4;
+    const T* cq = cc + ng[u] * 4;
+    const float dx = dt[u] * xd[u];
+    float4 v = hv[u];
+    v.x = fmaf(ex2(dt[u] * (a4[u].x * kLog2e)), v.x, dx * AT::ld(bq + 0));
+    v.y = fmaf(ex2(dt[u] * (a4[u].y * kLog2e)), v.y, dx * AT::ld(bq + 1));
+    v.z = fmaf(ex2(dt[u] * (a4[u].z * kLog2e)), v.z, dx * AT::ld(bq + 2));
+    v.w = fmaf(ex2(dt[u] * (a4[u].w * kLog2e)), v.w, dx * AT::ld(bq + 3));
+    if (ok[u]) *reinterpret_cast<float4*>(h + q * N + ng[u] * 4) = v;
+    float part = fmaf(AT::ld(cq + 0), v.x, fmaf(AT::ld(cq + 1), v.y, fmaf(AT::ld(cq + 2), v.z, AT::ld(cq + 3) * v.w)));
+#pragma unroll
+    for (int o = 1; o < NG; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (ok[u] && ng[u] == 0) {
+      const float zz = AT::ld(z + q);
+      const float s = fmaf(Dv[d[u]], xd[u], part);
+      const float o = s * zz * sigmoid(zz);
+      if constexpr (sizeof(T) == 4) y[q] = o;
+      else y[q] = __float2bfloat16_rn(o);
+    }
   }
 }
 
-template <int K, typename T, bool SILU>
+// CTA (blockIdx.x = sequence b, blockIdx.y = a run of kStepU * kStepThreads
+// channels): each thread shifts kStepU channels' registers, loads first.  With
+// VEC (K = 4, 16-byte aligned state) a channel's register is one 16-byte load
+// and store.
+template <int K, typename T, bool SILU, bool VEC>
 __global__ void __launch_bounds__(kStepThreads) conv_step_kernel(const T* __restrict__ x, float* __restrict__ state,
                                                                  const float* __restrict__ w,
                                                                  const float* __restrict__ bias, T* __restrict__ out,
                                                                  int B, int D) {
-  const long long q = (long long)blockIdx.x * kStepThreads + threadIdx.x;
-  if (q >= (long long)B * D) return;
-  const int d = (int)(q % D);
-  float st[K];
+  const int b = (int)blockIdx.x;
+  float st[kStepU][K], xv[kStepU];
+  int d[kStepU];
 #pragma unroll
-  for (int k = 0; k < K; ++k) st[k] = state[q * K + k];
+  for (int u = 0; u < kStepU; ++u) {
+    d[u] = ((int)blockIdx.y * kStepU + u) * kStepThreads + (int)threadIdx.x;
+    const size_t q = (size_t)b * D + d[u];
+    if (d[u] < D) {
+      if constexpr (VEC) {
+        const float4 v = *reinterpret_cast<const float4*>(state + q * K);
+        st[u][0] = v.x; st[u][1] = v.y; st[u][2] = v.z; st[u][3] = v.w;
+      } else {
 #pragma unroll
-  for (int k = 0; k < K - 1; ++k) st[k] = st[k + 1];
-  st[K - 1] = ActT<T>::ld(x + q);
-  float acc = bias != nullptr ? bias[d] : 0.f;
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    acc = fmaf(w[(size_t)d * K + k], st[k], acc);
-    state[q * K + k] = st[k];
+        for (int k = 0; k < K; ++k) st[u][k] = state[q * K + k];
+      }
+      xv[u] = ActT<T>::ld(x + q);
+    }
   }
-  if (SILU) acc = acc * sigmoid(acc);
-  if constexpr (sizeof(T) == 4) out[q] = acc;
-  else out[q] = __float2bfloat16_rn(acc);
+#pragma unroll
+  for (int u = 0; u < kStepU; ++u) {
+    if (d[u] >= D) continue;
+    const size_t q = (size_t)b * D + d[u];
+#pragma unroll
+    for (int k = 0; k < K - 1; ++k) st[u][k] = st[u][k + 1];
+    st[u][K - 1] = xv[u];
+    float acc = bias != nullptr ? bias[d[u]] : 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) acc = fmaf(w[(size_t)d[u] * K + k], st[u][k], acc);
+    if constexpr (VEC) {
+      *reinterpret_cast<float4*>(state + q * K) = make_float4(st[u][0], st[u][1], st[u][2], st[u][3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < K; ++k) state[q * K + k] = st[u][k];
+    }
+    if (SILU) acc = acc * sigmoid(acc);
+    if constexpr (sizeof(T) == 4) out[q] = acc;
+    else out[q] = __float2bfloat16_rn(acc);
+  }
 }
 
 template <int N, typename T>
 int step_launch(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm, const float* Dv,
                 const void* z, float* h, void* y, int B, int D, cudaStream_t s) {
-  const long long threads = (long long)B * D * (N / 4);
-  const long long blocks = (threads + kStepThreads - 1) / kStepThreads;
-  ss_step_kernel<N, T><<<(unsigned)blocks, kStepThreads, 0, s>>>(
+  const long long slots = (long long)D * (N / 4);  // per sequence
+  const long long runs = (slots + kStepU * kStepThreads - 1) / (kStepU * kStepThreads);
+  ss_step_kernel<N, T><<<dim3((unsigned)B, (unsigned)runs), kStepThreads, 0, s>>>(
       static_cast<const T*>(x), static_cast<const T*>(delta), A, static_cast<const T*>(Bm), static_cast<const T*>(Cm), Dv,
       static_cast<const T*>(z), h, static_cast<T*>(y), B, D);
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
@@ -98,11 +139,17 @@ int step_launch(const void* x, const void* delta, const float* A, const void* Bm
 template <int K, typename T>
 int conv_step_launch(const void* x, float* state, const float* w, const float* bias, void* out, int B, int D, int silu,
                      cudaStream_t s) {
-  const long long blocks = ((long long)B * D + kStepThreads - 1) / kStepThreads;
+  const dim3 grid((unsigned)B, (unsigned)((D + kStepU * kStepThreads - 1) / (kStepU * kStepThreads)));
   const T* xx = static_cast<const T*>(x);
   T* o = static_cast<T*>(out);
-  if (silu) conv_step_kernel<K, T, true><<<(unsigned)blocks, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
-  else conv_step_kernel<K, T, false><<<(unsigned)blocks, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
+  constexpr bool kVec = K == 4;
+  if (kVec && ssh::aligned16(state)) {
+    if (silu) conv_step_kernel<K, T, true, kVec><<<grid, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
+    else conv_step_kernel<K, T, false, kVec><<<grid, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
+  } else {
+    if (silu) conv_step_kernel<K, T, true, false><<<grid, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
+    else conv_step_kernel<K, T, false, false><<<grid, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
+  }
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
@@ -126,7 +173,7 @@ extern "C" int ss_scan_step(const void* x, const void* delta, const float* A, co
   if (B <= 0 || D <= 0 || N <= 0) return SS_ERR_DIM;
   if (N != 4 && N != 8 && N != 16) return SS_ERR_UNSUPPORTED;
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
-  if ((long long)B * D * (N / 4) >= (1ll << 38)) return SS_ERR_DIM;  // grid.x < 2^31 blocks
+  if ((long long)D * (N / 4) > 65535ll * kStepU * kStepThreads) return SS_ERR_DIM;  // grid.y <= 65535
   if (!ssh::aligned16(A) || !ssh::aligned16(h)) return SS_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SS_F32) {
@@ -145,7 +192,7 @@ extern "C" int conv1d_causal_step(const void* x, float* conv_state, const float*
   if (B <= 0 || D <= 0 || d_conv <= 0) return SS_ERR_DIM;
   if (d_conv > 4) return SS_ERR_UNSUPPORTED;
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
-  if ((long long)B * D >= (1ll << 38)) return SS_ERR_DIM;  // grid.x < 2^31 blocks
+  if ((long long)D > 65535ll * kStepU * kStepThreads) return SS_ERR_DIM;  // grid.y <= 65535
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SS_F32) return conv_step_dispatch<float>(x, conv_state, w, bias, out, B, D, d_conv, silu, s);
   return conv_step_dispatch<__nv_bfloat16>(x, conv_state, w, bias, out, B, D, d_conv, silu, s);
