@@ -24,7 +24,7 @@ constexpr int kStepThreads = 256;
 // state vectors, with all their loads issued before the arithmetic.
 constexpr int kStepU = 2;
 
-template <int N, typename T>
+template <int N, typename T, bool VBC>
 __global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const T* __restrict__ x, const T* __restrict__ delta,
                                                                const float* __restrict__ A, const T* __restrict__ Bm,
                                                                const T* __restrict__ Cm, const float* __restrict__ Dv,
@@ -56,14 +56,25 @@ __global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const T* __restri
     const size_t q = (size_t)b * D + (ok[u] ? d[u] : 0);
     const T* bq = bb + ng[u] * 4;
     const T* cq = cc + ng[u] * 4;
+    float bv[4], cv[4];  // one 8- or 16-byte load each when B_t / C_t rows are aligned for it
+    if constexpr (VBC) {
+      AT::ld4(bq, bv);
+      AT::ld4(cq, cv);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        bv[k] = AT::ld(bq + k);
+        cv[k] = AT::ld(cq + k);
+      }
+    }
     const float dx = dt[u] * xd[u];
     float4 v = hv[u];
-    v.x = fmaf(ex2(dt[u] * (a4[u].x * kLog2e)), v.x, dx * AT::ld(bq + 0));
-    v.y = fmaf(ex2(dt[u] * (a4[u].y * kLog2e)), v.y, dx * AT::ld(bq + 1));
-    v.z = fmaf(ex2(dt[u] * (a4[u].z * kLog2e)), v.z, dx * AT::ld(bq + 2));
-    v.w = fmaf(ex2(dt[u] * (a4[u].w * kLog2e)), v.w, dx * AT::ld(bq + 3));
+    v.x = fmaf(ex2(dt[u] * (a4[u].x * kLog2e)), v.x, dx * bv[0]);
+    v.y = fmaf(ex2(dt[u] * (a4[u].y * kLog2e)), v.y, dx * bv[1]);
+    v.z = fmaf(ex2(dt[u] * (a4[u].z * kLog2e)), v.z, dx * bv[2]);
+    v.w = fmaf(ex2(dt[u] * (a4[u].w * kLog2e)), v.w, dx * bv[3]);
     if (ok[u]) *reinterpret_cast<float4*>(h + q * N + ng[u] * 4) = v;
-    float part = fmaf(AT::ld(cq + 0), v.x, fmaf(AT::ld(cq + 1), v.y, fmaf(AT::ld(cq + 2), v.z, AT::ld(cq + 3) * v.w)));
+    float part = fmaf(cv[0], v.x, fmaf(cv[1], v.y, fmaf(cv[2], v.z, cv[3] * v.w)));
 #pragma unroll
     for (int o = 1; o < NG; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if (ok[u] && ng[u] == 0) {
@@ -130,7 +141,10 @@ int step_launch(const void* x, const void* delta, const float* A, const void* Bm
                 const void* z, float* h, void* y, int B, int D, cudaStream_t s) {
   const long long slots = (long long)D * (N / 4);  // per sequence
   const long long runs = (slots + kStepU * kStepThreads - 1) / (kStepU * kStepThreads);
-  ss_step_kernel<N, T><<<dim3((unsigned)B, (unsigned)runs), kStepThreads, 0, s>>>(
+  const uintptr_t quad = 4 * sizeof(T) - 1;  // a state quad of B_t / C_t: 8 bytes (bf16) or 16 (fp32)
+  const bool vbc = ((reinterpret_cast<uintptr_t>(Bm) | reinterpret_cast<uintptr_t>(Cm)) & quad) == 0;
+  auto kern = vbc ? ss_step_kernel<N, T, true> : ss_step_kernel<N, T, false>;
+  kern<<<dim3((unsigned)B, (unsigned)runs), kStepThreads, 0, s>>>(
       static_cast<const T*>(x), static_cast<const T*>(delta), A, static_cast<const T*>(Bm), static_cast<const T*>(Cm), Dv,
       static_cast<const T*>(z), h, static_cast<T*>(y), B, D);
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
