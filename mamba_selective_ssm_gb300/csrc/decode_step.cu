@@ -19,12 +19,13 @@ using namespace ssk;
 
 constexpr int kStepThreads = 256;
 
-// CTA (blockIdx.x = sequence b, blockIdx.y = a run of kStepU * kStepThreads
-// (channel, state quad) slots of that sequence): each thread advances kStepU
-// state vectors, with all their loads issued before the arithmetic.
-constexpr int kStepU = 2;
-
-template <int N, typename T, bool VBC>
+// CTA (blockIdx.x = sequence b, blockIdx.y = a run of U * kStepThreads
+// (channel, state quad) slots of that sequence): each thread advances U state
+// vectors, with all their loads issued before the arithmetic.  U = 2 when the
+// grid still has a few CTAs per SM (1024 sequences: 120.8 -> 115.6 us with the
+// vector B_t / C_t loads), 1 for a handful of sequences, whose latency is the
+// number of CTAs in flight.
+template <int N, typename T, bool VBC, int U>
 __global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const T* __restrict__ x, const T* __restrict__ delta,
                                                                const float* __restrict__ A, const T* __restrict__ Bm,
                                                                const T* __restrict__ Cm, const float* __restrict__ Dv,
@@ -35,13 +36,13 @@ __global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const T* __restri
   const int b = (int)blockIdx.x;
   const T* bb = Bm + (size_t)b * N;
   const T* cc = Cm + (size_t)b * N;
-  float4 hv[kStepU], a4[kStepU];
-  float dt[kStepU], xd[kStepU];
-  bool ok[kStepU];
-  int d[kStepU], ng[kStepU];
+  float4 hv[U], a4[U];
+  float dt[U], xd[U];
+  bool ok[U];
+  int d[U], ng[U];
 #pragma unroll
-  for (int u = 0; u < kStepU; ++u) {
-    const int slot = ((int)blockIdx.y * kStepU + u) * kStepThreads + (int)threadIdx.x;  // d * NG + ng
+  for (int u = 0; u < U; ++u) {
+    const int slot = ((int)blockIdx.y * U + u) * kStepThreads + (int)threadIdx.x;  // d * NG + ng
     d[u] = slot / NG;
     ng[u] = slot % NG;
     ok[u] = d[u] < D;
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const T* __restri
     hv[u] = ok[u] ? *reinterpret_cast<const float4*>(h + q * N + ng[u] * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
-  for (int u = 0; u < kStepU; ++u) {
+  for (int u = 0; u < U; ++u) {
     const size_t q = (size_t)b * D + (ok[u] ? d[u] : 0);
     const T* bq = bb + ng[u] * 4;
     const T* cq = cc + ng[u] * 4;
@@ -87,21 +88,21 @@ __global__ void __launch_bounds__(kStepThreads) ss_step_kernel(const T* __restri
   }
 }
 
-// CTA (blockIdx.x = sequence b, blockIdx.y = a run of kStepU * kStepThreads
-// channels): each thread shifts kStepU channels' registers, loads first.  With
-// VEC (K = 4, 16-byte aligned state) a channel's register is one 16-byte load
-// and store.
-template <int K, typename T, bool SILU, bool VEC>
+// CTA (blockIdx.x = sequence b, blockIdx.y = a run of U * kStepThreads
+// channels): each thread shifts U channels' registers, loads first.  With VEC
+// (K = 4, 16-byte aligned state) a channel's register is one 16-byte load and
+// store.
+template <int K, typename T, bool SILU, bool VEC, int U>
 __global__ void __launch_bounds__(kStepThreads) conv_step_kernel(const T* __restrict__ x, float* __restrict__ state,
                                                                  const float* __restrict__ w,
                                                                  const float* __restrict__ bias, T* __restrict__ out,
                                                                  int B, int D) {
   const int b = (int)blockIdx.x;
-  float st[kStepU][K], xv[kStepU];
-  int d[kStepU];
+  float st[U][K], xv[U];
+  int d[U];
 #pragma unroll
-  for (int u = 0; u < kStepU; ++u) {
-    d[u] = ((int)blockIdx.y * kStepU + u) * kStepThreads + (int)threadIdx.x;
+  for (int u = 0; u < U; ++u) {
+    d[u] = ((int)blockIdx.y * U + u) * kStepThreads + (int)threadIdx.x;
     const size_t q = (size_t)b * D + d[u];
     if (d[u] < D) {
       if constexpr (VEC) {
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(kStepThreads) conv_step_kernel(const T* __rest
     }
   }
 #pragma unroll
-  for (int u = 0; u < kStepU; ++u) {
+  for (int u = 0; u < U; ++u) {
     if (d[u] >= D) continue;
     const size_t q = (size_t)b * D + d[u];
 #pragma unroll
@@ -140,10 +141,13 @@ template <int N, typename T>
 int step_launch(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm, const float* Dv,
                 const void* z, float* h, void* y, int B, int D, cudaStream_t s) {
   const long long slots = (long long)D * (N / 4);  // per sequence
-  const long long runs = (slots + kStepU * kStepThreads - 1) / (kStepU * kStepThreads);
+  const long long runs2 = (slots + 2 * kStepThreads - 1) / (2 * kStepThreads);
+  const bool two = (long long)B * runs2 >= 2ll * device_sm_count();
+  const long long runs = two ? runs2 : (slots + kStepThreads - 1) / kStepThreads;
   const uintptr_t quad = 4 * sizeof(T) - 1;  // a state quad of B_t / C_t: 8 bytes (bf16) or 16 (fp32)
   const bool vbc = ((reinterpret_cast<uintptr_t>(Bm) | reinterpret_cast<uintptr_t>(Cm)) & quad) == 0;
-  auto kern = vbc ? ss_step_kernel<N, T, true> : ss_step_kernel<N, T, false>;
+  auto kern = two ? (vbc ? ss_step_kernel<N, T, true, 2> : ss_step_kernel<N, T, false, 2>)
+                  : (vbc ? ss_step_kernel<N, T, true, 1> : ss_step_kernel<N, T, false, 1>);
   kern<<<dim3((unsigned)B, (unsigned)runs), kStepThreads, 0, s>>>(
       static_cast<const T*>(x), static_cast<const T*>(delta), A, static_cast<const T*>(Bm), static_cast<const T*>(Cm), Dv,
       static_cast<const T*>(z), h, static_cast<T*>(y), B, D);
@@ -153,17 +157,20 @@ int step_launch(const void* x, const void* delta, const float* A, const void* Bm
 template <int K, typename T>
 int conv_step_launch(const void* x, float* state, const float* w, const float* bias, void* out, int B, int D, int silu,
                      cudaStream_t s) {
-  const dim3 grid((unsigned)B, (unsigned)((D + kStepU * kStepThreads - 1) / (kStepU * kStepThreads)));
+  const long long runs2 = (D + 2 * kStepThreads - 1) / (2 * kStepThreads);
+  const bool two = (long long)B * runs2 >= 2ll * device_sm_count();
+  const dim3 grid((unsigned)B, (unsigned)(two ? runs2 : (D + kStepThreads - 1) / kStepThreads));
   const T* xx = static_cast<const T*>(x);
   T* o = static_cast<T*>(out);
   constexpr bool kVec = K == 4;
-  if (kVec && ssh::aligned16(state)) {
-    if (silu) conv_step_kernel<K, T, true, kVec><<<grid, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
-    else conv_step_kernel<K, T, false, kVec><<<grid, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
-  } else {
-    if (silu) conv_step_kernel<K, T, true, false><<<grid, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
-    else conv_step_kernel<K, T, false, false><<<grid, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
-  }
+  const bool vec = kVec && ssh::aligned16(state);
+  using Kern = void (*)(const T*, float*, const float*, const float*, T*, int, int);
+  Kern kern;
+  if (vec) kern = silu ? (two ? conv_step_kernel<K, T, true, kVec, 2> : conv_step_kernel<K, T, true, kVec, 1>)
+                       : (two ? conv_step_kernel<K, T, false, kVec, 2> : conv_step_kernel<K, T, false, kVec, 1>);
+  else kern = silu ? (two ? conv_step_kernel<K, T, true, false, 2> : conv_step_kernel<K, T, true, false, 1>)
+                   : (two ? conv_step_kernel<K, T, false, false, 2> : conv_step_kernel<K, T, false, false, 1>);
+  kern<<<grid, kStepThreads, 0, s>>>(xx, state, w, bias, o, B, D);
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
@@ -187,7 +194,7 @@ extern "C" int ss_scan_step(const void* x, const void* delta, const float* A, co
   if (B <= 0 || D <= 0 || N <= 0) return SS_ERR_DIM;
   if (N != 4 && N != 8 && N != 16) return SS_ERR_UNSUPPORTED;
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
-  if ((long long)D * (N / 4) > 65535ll * kStepU * kStepThreads) return SS_ERR_DIM;  // grid.y <= 65535
+  if ((long long)D * (N / 4) > 65535ll * kStepThreads) return SS_ERR_DIM;  // grid.y <= 65535
   if (!ssh::aligned16(A) || !ssh::aligned16(h)) return SS_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SS_F32) {
@@ -206,7 +213,7 @@ extern "C" int conv1d_causal_step(const void* x, float* conv_state, const float*
   if (B <= 0 || D <= 0 || d_conv <= 0) return SS_ERR_DIM;
   if (d_conv > 4) return SS_ERR_UNSUPPORTED;
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
-  if ((long long)D > 65535ll * kStepU * kStepThreads) return SS_ERR_DIM;  // grid.y <= 65535
+  if ((long long)D > 65535ll * kStepThreads) return SS_ERR_DIM;  // grid.y <= 65535
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SS_F32) return conv_step_dispatch<float>(x, conv_state, w, bias, out, B, D, d_conv, silu, s);
   return conv_step_dispatch<__nv_bfloat16>(x, conv_state, w, bias, out, B, D, d_conv, silu, s);
