@@ -18,7 +18,8 @@
 // each incoming dout[t] into g[t] = dout[t] * silu'(pre[t]) with
 // pre[t] = bias + sum_k w[k] x[t-(K-1)+k] recomputed from the x window behind
 // t, and completes dx[t-(K-1)] from the last K values of g; the loads of eight
-// steps are issued together, at three CTAs per SM.  The four-channel arithmetic runs as packed
+// steps are issued together, at three CTAs per SM (with fp32 x, 2 channels per
+// thread at six CTAs per SM).  The four-channel arithmetic runs as packed
 // f32x2 operations (two per step where scalar code takes four).
 #include "common.cuh"
 
@@ -210,6 +211,91 @@ __global__ void __launch_bounds__(kCThreads, SILU ? kCtasSilu : 4) conv_bwd_kern
   }
 }
 
+// The SiLU-fused backward with 2 channels per thread (twice the threads of the
+// 4-channel form, half the registers each), for fp32 x and rows of at least 256
+// channels: the same input-step walk, loads of U steps issued together.
+constexpr int kCtasSilu2 = 6;
+
+template <int K>
+__global__ void __launch_bounds__(kCThreads, kCtasSilu2) conv_silu_bwd2_kernel(const float* __restrict__ dout,
+                                                                              const float* __restrict__ x,
+                                                                              const float* __restrict__ w,
+                                                                              const float* __restrict__ bias,
+                                                                              float* __restrict__ dx,
+                                                                              float* __restrict__ ws, int B, int L,
+                                                                              int D) {
+  pdl_trigger();  // the column sum of the partials may launch now; it waits for this grid's end
+  constexpr int TILE = kCTileSilu;
+  constexpr int U = 8;
+  const int d = (int)(blockIdx.x * kCThreads + threadIdx.x) * 2;
+  const bool valid = d < D;  // D % 8 == 0: both channels of a thread are in range
+  const int ntt = (L + TILE - 1) / TILE;
+  float2 wk[K], dw[K], db = f2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    wk[k] = valid ? f2(w[(size_t)d * K + k], w[(size_t)(d + 1) * K + k]) : f2(0.f, 0.f);
+    dw[k] = f2(0.f, 0.f);
+  }
+  const float2 b2 = (valid && bias != nullptr) ? *reinterpret_cast<const float2*>(bias + d) : f2(0.f, 0.f);
+  if (valid) {
+    for (int bt = blockIdx.y; bt < B * ntt; bt += gridDim.y) {
+      const int b = bt / ntt, t0 = (bt % ntt) * TILE;
+      const int t1 = min(L, t0 + TILE);
+      const int tend = t1 + K - 1, tl = min(L, tend);
+      const float* g = dout + (size_t)b * L * D + d;
+      const float* xb = x + (size_t)b * L * D + d;
+      float2 xw[K], gw[K];  // xw[k] = x[t-(K-1)+k], gw[j] = g[t-(K-1)+j]
+#pragma unroll
+      for (int j = 0; j < K - 1; ++j) {
+        const int tx = t0 - (K - 1) + j;
+        xw[j + 1] = tx >= 0 ? *reinterpret_cast<const float2*>(xb + (size_t)tx * D) : f2(0.f, 0.f);
+        gw[j + 1] = f2(0.f, 0.f);  // only ever combined into outputs before t0
+      }
+      for (int tb = t0; tb < tend; tb += U) {
+        float2 gr[U], xr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const bool in = tb + u < tl;
+          gr[u] = in ? *reinterpret_cast<const float2*>(g + (size_t)(tb + u) * D) : f2(0.f, 0.f);
+          xr[u] = in ? *reinterpret_cast<const float2*>(xb + (size_t)(tb + u) * D) : f2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int t = tb + u;
+          if (t < tend) {
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j) {
+              xw[j] = xw[j + 1];
+              gw[j] = gw[j + 1];
+            }
+            xw[K - 1] = xr[u];
+            float2 pre = b2;
+#pragma unroll
+            for (int k = 0; k < K; ++k) pre = fma2(wk[k], xw[k], pre);
+            gw[K - 1] = gdsilu2(gr[u], pre);
+            if (t < t1) {
+#pragma unroll
+              for (int k = 0; k < K; ++k) dw[k] = fma2(gw[K - 1], xw[k], dw[k]);
+              db = add2(db, gw[K - 1]);
+            }
+            const int sdx = t - (K - 1);
+            if (sdx >= t0) {
+              float2 acc = f2(0.f, 0.f);
+#pragma unroll
+              for (int j = 0; j < K; ++j) acc = fma2(gw[j], wk[K - 1 - j], acc);
+              *reinterpret_cast<float2*>(dx + ((size_t)b * L + sdx) * D + d) = acc;
+            }
+          }
+        }
+      }
+    }
+    float* o = ws + (size_t)blockIdx.y * (K + 1) * D + d;  // partial row: [K+1][D]
+#pragma unroll
+    for (int k = 0; k < K; ++k) *reinterpret_cast<float2*>(o + (size_t)k * D) = dw[k];
+    *reinterpret_cast<float2*>(o + (size_t)K * D) = db;
+  }
+}
+
 // column i = k * D + d of the partials: dw[d, k] (k < K) or db[d] (k = K)
 struct ConvStore {
   float* dw;
@@ -253,6 +339,22 @@ int conv_validate(int B, int L, int D, int K, int x_dtype) {
 template <int K, typename T, bool SILU>
 int conv_launch(const float* dout, const void* x, const float* w, const float* bias, float* dx, float* dw, float* db,
                 int B, int L, int D, float* ws, const ConvPlan& pl, cudaStream_t s) {
+  // fp32 x: two channels per thread, one wave of kCtasSilu2 CTAs per SM (mamba130m 70 -> 64 us); bf16 x keeps four
+  // (its two-channel loads of x would be 4 bytes: 81 -> 99 us on the 1.4B layer)
+  if constexpr (SILU && sizeof(T) == 4) {
+    if (D >= 2 * kCThreads) {
+      const int gx2 = (D / 2 + kCThreads - 1) / kCThreads;
+      int gy2 = (kCtasSilu2 * device_sm_count()) / gx2;
+      if (gy2 < 1) gy2 = 1;
+      if (gy2 > pl.rows) gy2 = pl.rows;  // the workspace holds pl.rows partial rows
+      const long long items = (long long)B * ((L + kCTileSilu - 1) / kCTileSilu);
+      if (gy2 > items) gy2 = (int)items;
+      conv_silu_bwd2_kernel<K><<<dim3(gx2, gy2), kCThreads, 0, s>>>(dout, static_cast<const float*>(x), w, bias, dx, ws,
+                                                                     B, L, D);
+      if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+      return colsum(ws, (long long)D * (K + 1), gy2, ConvStore{dw, db, D, K}, s) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    }
+  }
   // one wave: the SiLU-fused form holds three CTAs per SM, so it runs fewer CTA rows (and partial rows)
   int gy = pl.gy, rows = pl.rows;
   if (SILU) {
